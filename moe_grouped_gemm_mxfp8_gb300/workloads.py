@@ -1,0 +1,247 @@
+"""Seeded synthetic inputs for MXFP8 grouped-matmul-finalize-routing.
+
+This module only draws random inputs.  It holds none of the operator's
+arithmetic, so the oracle and the CUDA path can both be fed from it without
+sharing any part of the computation.
+
+Tensor roles and shapes follow the operator's input table ("MXFP8 实现与精度验证"
+write-up, section 3.1, and the aclnnGroupedMatmulFinalizeRoutingV3 parameter
+constraints):
+
+    x1              [M, K]                 FP8 bytes (E4M3FN or E5M2), routed tokens
+    x2              [E, K, N] or [E, N, K] FP8 bytes, expert weights (transpose_x2)
+    scale           [ceil(K/64), N, 2] or [N, ceil(K/64), 2] E8M0 bytes
+                    (optionally with a leading E dimension, one slice per expert)
+    pertoken_scale  [M, ceil(K/64), 2]     E8M0 bytes
+    group_list      [E] int64              prefix sums (type 0) or counts (type 1)
+    logit           [M] float32
+    row_index       [M] int64              values in [0, batch)
+    shared_input    [rows, N] bfloat16
+    out             [batch, N] float32     initial value, accumulated into
+
+The input construction mirrors the write-up's test builder (section 3.3:
+randn cast to FP8, scales stored as E8M0 bytes, row_index = arange(M) % batch,
+bf16 shared input, FP32 zeros for out) and the five workload recipes that the
+benchmark and the parity tests use.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Optional
+
+import torch
+
+E4M3 = 0
+E5M2 = 1
+
+_TORCH_FP8 = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
+
+
+@dataclasses.dataclass
+class Spec:
+    """One problem: sizes, formats and the recipe for its random inputs."""
+
+    name: str
+    batch: int
+    M: int
+    K: int
+    N: int
+    E: int
+    x1_dtype: int = E4M3
+    x2_dtype: int = E4M3
+    transpose_x2: bool = False
+    scale_per_expert: bool = False
+    group_list_type: int = 1
+    # token distribution over experts: "uniform" (equal counts, remainder on
+    # the leading experts), "multinomial" (uniform probabilities), "zipf"
+    # (probabilities proportional to (i+1)^-zipf_s), or "explicit"
+    counts: str = "uniform"
+    zipf_s: float = 1.2
+    explicit_counts: Optional[tuple] = None
+    scale_lo: int = 124
+    scale_hi: int = 130
+    # row_index recipe: "mod" (arange % batch), "random" (uniform in [0,batch)),
+    # "topk" (t // topk)
+    rows: str = "mod"
+    topk: int = 1
+    # logit recipe: "uniform" U(0,1), "softmax" (softmax of topk normals per row), "none"
+    logit: str = "uniform"
+    shared_rows: Optional[int] = None  # None -> batch; 0 -> no shared input
+    shared_offset: int = 0
+    shared_weight: float = 1.0
+    out_init: str = "zeros"  # "zeros" | "randn"
+    seed: int = 0
+
+    @property
+    def Ks(self) -> int:
+        return (self.K + 63) // 64
+
+    @property
+    def n_shared(self) -> int:
+        return self.batch if self.shared_rows is None else self.shared_rows
+
+
+def _gen(device: str, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def expert_counts(spec: Spec) -> torch.Tensor:
+    """Tokens per expert (int64 [E]) for the spec's routing recipe."""
+    E, M = spec.E, spec.M
+    if spec.counts == "explicit":
+        c = torch.tensor(spec.explicit_counts, dtype=torch.int64)
+        assert c.numel() == E
+        return c
+    if spec.counts == "uniform":
+        base, rem = divmod(M, E)
+        return torch.tensor([base + (1 if i < rem else 0) for i in range(E)], dtype=torch.int64)
+    g = _gen("cpu", spec.seed * 7919 + 17)
+    if spec.counts == "multinomial":
+        p = torch.full((E,), 1.0 / E, dtype=torch.float64)
+    elif spec.counts == "zipf":
+        p = torch.tensor([(i + 1) ** (-spec.zipf_s) for i in range(E)], dtype=torch.float64)
+        p = p / p.sum()
+    else:
+        raise ValueError(spec.counts)
+    draws = torch.multinomial(p, M, replacement=True, generator=g)
+    return torch.bincount(draws, minlength=E).to(torch.int64)
+
+
+def group_list_from_counts(counts: torch.Tensor, group_list_type: int) -> torch.Tensor:
+    """Encode per-expert counts as the operator's group_list (type 0 prefix sums, type 1 counts)."""
+    if group_list_type == 1:
+        return counts.clone()
+    if group_list_type == 0:
+        return torch.cumsum(counts, 0).to(torch.int64)
+    raise ValueError(group_list_type)
+
+
+def _fp8_bytes(shape, dtype_code: int, g: torch.Generator, device: str) -> torch.Tensor:
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    return x.to(_TORCH_FP8[dtype_code]).view(torch.uint8)
+
+
+def _e8m0_bytes(shape, lo: int, hi: int, g: torch.Generator, device: str) -> torch.Tensor:
+    return torch.randint(lo, hi + 1, shape, generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+
+
+def make_inputs(spec: Spec, device: str = "cpu", weights_device: Optional[str] = None) -> Dict[str, torch.Tensor]:
+    """Draw every input of one call.  Small tensors are drawn on the CPU from
+    fixed seeds; the weight tensor x2 (up to several GB) is drawn on
+    ``weights_device`` (default: ``device``) with its own seeded generator."""
+    weights_device = weights_device or device
+    g = _gen("cpu", spec.seed)
+    M, K, N, E, Ks = spec.M, spec.K, spec.N, spec.E, spec.Ks
+
+    x1 = _fp8_bytes((M, K), spec.x1_dtype, g, "cpu")
+    gw = _gen(weights_device, spec.seed + 100003)
+    wshape = (E, N, K) if spec.transpose_x2 else (E, K, N)
+    x2 = _fp8_bytes(wshape, spec.x2_dtype, gw, weights_device)
+
+    sshape = (N, Ks, 2) if spec.transpose_x2 else (Ks, N, 2)
+    if spec.scale_per_expert:
+        sshape = (E,) + sshape
+    scale = _e8m0_bytes(sshape, spec.scale_lo, spec.scale_hi, g, "cpu")
+    pertoken_scale = _e8m0_bytes((M, Ks, 2), spec.scale_lo, spec.scale_hi, g, "cpu")
+
+    counts = expert_counts(spec)
+    assert int(counts.sum()) <= M
+    group_list = group_list_from_counts(counts, spec.group_list_type)
+
+    if spec.logit == "uniform":
+        logit = torch.rand((M,), generator=g, dtype=torch.float32)
+    elif spec.logit == "softmax":
+        z = torch.randn((math.ceil(M / spec.topk), spec.topk), generator=g, dtype=torch.float32)
+        logit = torch.softmax(z, dim=1).reshape(-1)[:M].contiguous()
+    elif spec.logit == "none":
+        logit = None
+    else:
+        raise ValueError(spec.logit)
+
+    if spec.rows == "mod":
+        row_index = torch.arange(M, dtype=torch.int64) % max(spec.batch, 1)
+    elif spec.rows == "random":
+        row_index = torch.randint(0, spec.batch, (M,), generator=g, dtype=torch.int64)
+    elif spec.rows == "topk":
+        row_index = torch.arange(M, dtype=torch.int64) // spec.topk
+    else:
+        raise ValueError(spec.rows)
+
+    R = spec.n_shared
+    shared_input = torch.randn((R, N), generator=g, dtype=torch.float32).to(torch.bfloat16) if R > 0 else None
+
+    if spec.out_init == "zeros":
+        out = torch.zeros((spec.batch, N), dtype=torch.float32)
+    elif spec.out_init == "randn":
+        out = torch.randn((spec.batch, N), generator=g, dtype=torch.float32)
+    else:
+        raise ValueError(spec.out_init)
+
+    d = dict(x1=x1, x2=x2, scale=scale, pertoken_scale=pertoken_scale, group_list=group_list,
+             logit=logit, row_index=row_index, shared_input=shared_input, out=out)
+    if device != "cpu":
+        d = {k: (v.to(device) if v is not None else None) for k, v in d.items()}
+    return d
+
+
+def _first_seed_with_empty_expert(spec: Spec, start: int) -> int:
+    s = start
+    while True:
+        if int((expert_counts(dataclasses.replace(spec, seed=s)) == 0).sum()) > 0:
+            return s
+        s += 1
+
+
+def config(i: int) -> Spec:
+    """The five benchmark workloads (1-based), by their sizes and recipes.
+
+    1: batch 64, topk 2, K 5120, N 4096, E 8, E4M3, counts 16/expert (type 1)
+    2: batch 128, topk 2, K 7168, N 4096, E 16, E4M3, x2 transposed, shared weight 0.5, out randn
+    3: batch 256, topk 3, K 8192, N 4096, E 32, E5M2, prefix sums (type 0), scales 120..134
+    4: batch 256, topk 3, K 7168, N 4096, E 32, E4M3, Zipf(1.2) counts, random rows,
+       shared 128 rows at offset 64 with weight 0.7
+    5: batch 512, topk 8, K 7168, N 4096, E 256, E4M3, multinomial counts, rows t//8,
+       softmax logits over the 8 tokens of a row
+    """
+    if i == 1:
+        return Spec("C1 M128 K5120 N4096 E8", batch=64, M=128, K=5120, N=4096, E=8, seed=1001)
+    if i == 2:
+        return Spec("C2 M256 K7168 N4096 E16 transposed", batch=128, M=256, K=7168, N=4096, E=16,
+                    transpose_x2=True, shared_weight=0.5, out_init="randn", seed=1002)
+    if i == 3:
+        return Spec("C3 M768 K8192 N4096 E32 E5M2", batch=256, M=768, K=8192, N=4096, E=32,
+                    x1_dtype=E5M2, x2_dtype=E5M2, group_list_type=0, scale_lo=120, scale_hi=134, seed=1003)
+    if i == 4:
+        s = Spec("C4 M768 K7168 N4096 E32 zipf", batch=256, M=768, K=7168, N=4096, E=32,
+                 counts="zipf", zipf_s=1.2, rows="random", shared_rows=128, shared_offset=64,
+                 shared_weight=0.7, seed=1004)
+        return dataclasses.replace(s, seed=_first_seed_with_empty_expert(s, 1004))
+    if i == 5:
+        return Spec("C5 M4096 K7168 N4096 E256", batch=512, M=4096, K=7168, N=4096, E=256,
+                    counts="multinomial", rows="topk", topk=8, logit="softmax", seed=1005)
+    raise ValueError(i)
+
+
+def algorithmic_bytes(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:
+    """Bytes a single call must move at minimum: x2 (and its scales) of every
+    expert that holds a token, x1, pertoken_scale, logit, row_index,
+    group_list, shared_input, and out read once and written once."""
+    if counts is None:
+        counts = expert_counts(spec)
+    nnz = int((counts > 0).sum())
+    covered = min(int(counts.sum()), spec.M)
+    K, N, Ks = spec.K, spec.N, spec.Ks
+    w = nnz * K * N + nnz * Ks * N * 2 if spec.scale_per_expert else nnz * K * N + Ks * N * 2
+    tok = covered * K + covered * Ks * 2 + covered * 4 * (0 if spec.logit == "none" else 1) + covered * 8
+    shared = spec.n_shared * N * 2
+    out = spec.batch * N * 4 * 2
+    return w + tok + shared + out + spec.E * 8
+
+
+def flops(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:
+    if counts is None:
+        counts = expert_counts(spec)
+    return 2 * min(int(counts.sum()), spec.M) * spec.N * spec.K
