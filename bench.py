@@ -1,0 +1,318 @@
+"""Benchmark of MXFP8 grouped-matmul-finalize-routing on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--deterministic] [--impl ours|reference]
+
+One step = one call of gmmfr_grouped_matmul_finalize_routing (prologue, grouped
+GEMM with the fused logit / scatter / shared epilogue, and in deterministic
+mode the row-ordered combine) on the chosen workload, weights prepared once
+beforehand (the preparation is timed separately).  `value` is the effective
+HBM bandwidth: algorithmic bytes (x2 and scales of experts holding tokens, x1,
+token scales, logit, row_index, group_list, shared_input, out read + written)
+over the device time of the call.  L2 is flushed (256 MB written) between
+steps, outside the timed events.  Multi-GPU runs are independent replicas.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and achieved HBM GB/s vs roofline, MXFP8 grouped-matmul-finalize-routing"
+DEFAULT_CONFIG = 2
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def _config_dict(spec, counts, deterministic):
+    return {"workload": spec.name, "M": spec.M, "K": spec.K, "N": spec.N, "E": spec.E, "batch": spec.batch,
+            "x1": "E5M2" if spec.x1_dtype else "E4M3", "x2": "E5M2" if spec.x2_dtype else "E4M3",
+            "transpose_x2": spec.transpose_x2, "group_list_type": spec.group_list_type,
+            "nonempty_experts": int((counts > 0).sum()), "max_tokens_per_expert": int(counts.max()),
+            "mode": "deterministic" if deterministic else "atomic",
+            "l2": "flushed between steps (256 MB write), weights also larger than L2",
+            "parallelism": "replicas"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gmmfr_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        try:
+            rows = [l.split(",") for l in open(self.path).read().strip().splitlines() if l.strip()]
+        except OSError:
+            return None
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for nm, v in zip(names, r[5:9]):
+                if v.strip() == "Active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def _cpu_baseline(spec, inp, target_s=10.0):
+    """The oracle, as it stands, on a column slice of the workload (all host
+    cores); returns (GB/s scaled to the whole workload, seconds, sample text, cores)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+    threads = oracle.num_threads()
+    ncols = min(spec.N, 64 * max(1, threads))
+    x2 = inp["x2"].cpu()
+    sc = inp["scale"].cpu()
+    if spec.transpose_x2:
+        x2s = x2[:, :ncols, :].contiguous()
+        scs = sc[..., :ncols, :, :].contiguous()
+    else:
+        x2s = x2[:, :, :ncols].contiguous()
+        scs = sc[..., :ncols, :].contiguous()
+    shared = inp["shared_input"][:, :ncols].contiguous() if inp["shared_input"] is not None else None
+    p = oracle.Problem(M=spec.M, K=spec.K, N=ncols, E=spec.E, batch=spec.batch, x1=inp["x1"].cpu(), x2=x2s,
+                       scale=scs, pertoken_scale=inp["pertoken_scale"].cpu(), group_list=inp["group_list"].cpu(),
+                       row_index=inp["row_index"].cpu(), out=inp["out"].cpu()[:, :ncols].contiguous(),
+                       x1_dtype=spec.x1_dtype, x2_dtype=spec.x2_dtype, transpose_x2=spec.transpose_x2,
+                       scale_per_expert=spec.scale_per_expert, group_list_type=spec.group_list_type,
+                       logit=inp["logit"].cpu() if inp["logit"] is not None else None, shared_input=shared,
+                       shared_offset=spec.shared_offset, shared_weight=spec.shared_weight)
+    t0 = time.perf_counter()
+    oracle.run(p)
+    dt = time.perf_counter() - t0
+    full_s = dt * spec.N / ncols
+    gbs = W.algorithmic_bytes(spec) / full_s / 1e9
+    return gbs, dt, f"oracle on output columns [0,{ncols}) of {spec.N} ({dt:.1f} s), scaled by N/{ncols}", threads
+
+
+def run_reference(args):
+    """The oracle (CPU) as the reference arm: each step is a bounded column sample."""
+    import torch
+
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    spec = W.config(args.config)
+    inp = W.make_inputs(spec)
+    counts = W.expert_counts(spec)
+    vals = []
+    sample = ""
+    cores = 1
+    for i in range(args.warmup + args.steps):
+        gbs, dt, sample, cores = _cpu_baseline(spec, inp)
+        if i >= args.warmup:
+            vals.append(gbs)
+    v = statistics.median(vals)
+    full_ms = W.algorithmic_bytes(spec) / (v * 1e9) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config_dict(spec, counts, args.deterministic),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from moe_grouped_gemm_mxfp8_gb300 import binding as B
+    from moe_grouped_gemm_mxfp8_gb300 import build as build_mod
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    build_mod.build()
+    B.load()
+
+    spec = W.config(args.config)
+    counts = W.expert_counts(spec)
+    alg_bytes = W.algorithmic_bytes(spec, counts)
+    flops = W.flops(spec, counts)
+    inp = W.make_inputs(spec, device="cpu", weights_device="cuda")
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    prob = B.problem_from_spec(spec, args.deterministic)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    # one-time weight preparation, timed on its own
+    n_prep = B.gmmfr_prepared_weights_size(prob)
+    prep = torch.empty(n_prep, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(2):
+        e0.record()
+        B.gmmfr_prepare_weights(prob, d["x2"].data_ptr(), d["scale"].data_ptr(), prep.data_ptr(), n_prep, sptr)
+        e1.record()
+    torch.cuda.synchronize()
+    prep_ms = e0.elapsed_time(e1)
+    ws = B.workspace(prob, True, "cuda")
+    out0 = d["out"].clone()
+    out = d["out"].clone()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def call(o):
+        B.run(prob, d, o, prepared=prep, ws=ws)
+
+    for _ in range(args.warmup):
+        call(out)
+    torch.cuda.synchronize()
+    bits = B.gmmfr_check_device_errors(ws.data_ptr(), sptr)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    B.gmmfr_profile_begin(args.steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            out.copy_(out0)
+            starts[i].record()
+            call(out)
+            ends[i].record()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    kernel_ms = B.gmmfr_profile_end(args.steps)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    gemm_ms = statistics.mean(k[2] for k in kernel_ms)
+    pro_ms = statistics.mean(k[1] for k in kernel_ms)
+    comb = [k[3] for k in kernel_ms if k[3] >= 0]
+    comb_ms = statistics.mean(comb) if comb else None
+
+    # end to end through the public call with host buffers: H2D of the step's
+    # inputs from pinned memory, the call, D2H of the result
+    per_step = ["x1", "pertoken_scale", "group_list", "logit", "row_index", "shared_input", "out"]
+    host = {k: inp[k].pin_memory() for k in per_step if inp[k] is not None}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    out_host = torch.empty_like(host["out"]).pin_memory()
+    d2h = out_host.numel() * out_host.element_size()
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    ee0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ee1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        if i >= args.warmup:
+            flush.zero_()
+            ee0[i - args.warmup].record()
+        for k, v in host.items():
+            dev[k].copy_(v, non_blocking=True)
+        dd = dict(d)
+        dd.update(dev)
+        B.run(prob, dd, dev["out"], prepared=prep, ws=ws)
+        out_host.copy_(dev["out"], non_blocking=True)
+        if i >= args.warmup:
+            ee1[i - args.warmup].record()
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ee0, ee1))
+
+    peaks, peak_kind = _peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    gbs = alg_bytes / (ms * 1e-3) / 1e9 * world
+    gemm_gbs = alg_bytes / (gemm_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp8 (fp8 x fp8, e8m0 per 32) -> f32", "data": "synthetic",
+        "config": _config_dict(spec, counts, args.deterministic),
+        "us_per_call": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12,
+        "roofline_fraction_call": gbs / world / hbm_peak,
+        "kernels_ms": {"prologue": pro_ms, "gemm": gemm_ms, "combine": comb_ms},
+        "weight_prep_ms": prep_ms,
+        "weight_prep_gbs": 2 * n_prep / (prep_ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": gemm_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gemm_gbs / hbm_peak, "traffic": None,
+                     "kernel": "gemm_kernel (grouped GEMM + fused epilogue)",
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
+        "e2e": {"value": alg_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (3 if args.deterministic else 2),
+        "device_error_bits": bits,
+        "clocks": clk.summary(),
+        "wall_s_timed": t_wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cgbs, cdt, sample, cores = _cpu_baseline(spec, inp)
+        line["cpu_baseline"] = {"value": cgbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * gmmfr — MXFP8 grouped matmul + finalize routing on one GB300 (sm_103a).
+ *
+ * The operator (grouped_matmul_finalize_routing MXFP8 write-up, czykbl.com/news/94077,
+ * sections 2.1-2.2 and 3.1; aclnnGroupedMatmulFinalizeRoutingV3, "计算公式" items 1-4):
+ *
+ *   for each expert e, for each routed token t in e's range and each column n:
+ *     mm(t,n)  = sum_k fp8(x1[t,k]) 2^(pertoken_scale[t,k/64,(k/32)%2]-127)
+ *                     * fp8(x2[e,k,n]) 2^(scale[k/64,n,(k/32)%2]-127)        (stage 1)
+ *     out[row_index[t], n] += logit[t] * mm(t,n)                             (stages 2, 3)
+ *   out[shared_input_offset + i, n] += shared_input_weight * shared_input[i, n]  (stage 4)
+ *
+ * One E8M0 scale covers 32 consecutive K elements; the [ceil(K/64), 2] pair
+ * layout is read as pair k/64, half (k/32)%2 (the write-up's golden expands
+ * scales by 32 along K, section 6.3).
+ *
+ * Conventions for every entry point:
+ *   - Tensor arguments are DEVICE pointers to dense row-major data owned by the
+ *     caller; the library keeps no pointer after a call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued on it; no entry point synchronises unless it says so.
+ *   - A call that returns an error status enqueues no work.  The message of the
+ *     last error on the calling thread is available from gmmfr_last_error().
+ *   - No entry point allocates device memory: scratch space is the caller's
+ *     `workspace`, and prepared weights live in a caller buffer.
+ */
+#ifndef GMMFR_H
+#define GMMFR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GMMFR_API __attribute__((visibility("default")))
+#else
+#define GMMFR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GMMFR_OK = 0,
+  GMMFR_ERR_INVALID_ARG = 1, /* a size, pointer, dtype code or offset is out of range */
+  GMMFR_ERR_UNSUPPORTED = 2, /* valid for the operator but not handled here (e.g. K % 16 != 0) */
+  GMMFR_ERR_WORKSPACE = 3,   /* workspace or prepared buffer too small or misaligned */
+  GMMFR_ERR_CUDA = 4,        /* a CUDA runtime call failed (no device, launch error, ...) */
+  GMMFR_ERR_DEVICE = 5       /* a device-side check failed; see gmmfr_check_device_errors */
+} gmmfr_status;
+
+/* FP8 element formats of x1 and x2 (section 3.1: FP8 E4M3/E5M2). */
+typedef enum { GMMFR_E4M3 = 0, GMMFR_E5M2 = 1 } gmmfr_fp8_format;
+
+/* Integer type of row_index: int64 as in the tensor table, or int32. */
+typedef enum { GMMFR_INDEX_I64 = 0, GMMFR_INDEX_I32 = 1 } gmmfr_index_type;
+
+/* problem.flags */
+#define GMMFR_DETERMINISTIC 1u /* row-ordered combine; bit-identical results run to run */
+
+/* Bits of the device error word (gmmfr_check_device_errors). */
+#define GMMFR_DEV_BAD_GROUP_LIST 1u /* negative count, decreasing prefix sum, or total > M; ranges were clamped */
+#define GMMFR_DEV_BAD_ROW_INDEX 2u  /* a routed token had row_index outside [0, batch); it was skipped */
+#define GMMFR_DEV_TIMEOUT 4u        /* a pipeline wait gave up; the output is incomplete */
+
+/*
+ * Sizes, formats and scalar arguments of one call (section 3.1 tensor table and
+ * section 5.1 FinalizeRoutingConfig fields).
+ *
+ *   M      rows of x1, pertoken_scale, logit, row_index (routed tokens, batch*topk); M >= 0
+ *   K      contraction length, K >= 1 (this build needs K % 16 == 0)
+ *   N      output columns, N >= 0
+ *   E      experts, 1 <= E <= 1024 (aclnn V3 constraint "e <= 1024")
+ *   batch  rows of out, batch >= 0
+ *   x1_format, x2_format     gmmfr_fp8_format of x1 and x2
+ *   transpose_x2             0: x2 [E,K,N], scale [ceil(K/64),N,2];
+ *                            1: x2 [E,N,K], scale [N,ceil(K/64),2] (scale follows x2, section 5.3)
+ *   scale_per_expert         1: scale carries a leading [E] dimension (aclnn's 4-D form)
+ *   group_list_type          0: prefix sums, expert e owns [g[e-1], g[e]) with g[-1] = 0;
+ *                            1: counts, expert e owns [sum g[:e], sum g[:e] + g[e]) (section 4.3)
+ *   row_index_type           gmmfr_index_type
+ *   shared_rows              rows of shared_input (0: no shared input)
+ *   shared_offset            first out row of the shared add; 0 <= offset, offset + rows <= batch
+ *   shared_weight            multiplier of shared_input (default 1.0 on the page)
+ *   flags                    GMMFR_DETERMINISTIC or 0
+ */
+typedef struct {
+  int64_t M, K, N, E, batch;
+  int32_t x1_format, x2_format;
+  int32_t transpose_x2;
+  int32_t scale_per_expert;
+  int32_t group_list_type;
+  int32_t row_index_type;
+  int64_t shared_rows;
+  int64_t shared_offset;
+  float shared_weight;
+  uint32_t flags;
+} gmmfr_problem;
+
+/*
+ * Bytes of the prepared-weight buffer for this problem's x2 and scale
+ * (E x ceil(N/128) x ceil(K/128) tiles of 16896 bytes).  Host only; no CUDA call.
+ * Returns GMMFR_ERR_INVALID_ARG on an invalid problem.
+ */
+GMMFR_API gmmfr_status gmmfr_prepared_weights_size(const gmmfr_problem* problem, size_t* bytes);
+
+/*
+ * One-time weight preparation: re-lays x2 and its E8M0 scale into the tiled,
+ * swizzled layout the grouped GEMM streams (one 128-column x 128-K tile of FP8
+ * weights followed by its 512 scale bytes), so that each tile is a single
+ * contiguous HBM read.  Inputs as in section 3.1 (x2 [E,K,N] or [E,N,K]; scale
+ * [(E,)ceil(K/64),N,2] or [(E,)N,ceil(K/64),2]).
+ *   prepared        device buffer of at least gmmfr_prepared_weights_size bytes,
+ *                   16-byte aligned, caller-owned; fully overwritten.
+ * Enqueued on `stream`; the buffer stays valid as long as the caller keeps it.
+ */
+GMMFR_API gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const void* x2, const void* scale,
+                                   void* prepared, size_t prepared_bytes, void* stream);
+
+/*
+ * Workspace bytes one call needs (two-phase use as in aclnn's
+ * GetWorkspaceSize/execute pair).  `have_prepared` = 0 adds room to prepare
+ * the weights inside the call.  Host only; may query the current device's SM
+ * count.  The workspace must be 256-byte aligned.
+ */
+GMMFR_API gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int have_prepared, size_t* bytes);
+
+/*
+ * The operator.  Enqueues the whole computation on `stream`; never syncs and
+ * never allocates.
+ *   x1              [M,K] FP8 bytes, 16-byte aligned
+ *   x2, scale       raw weights and their scales; read only when prepared == NULL
+ *                   (they are then prepared into the workspace first)
+ *   pertoken_scale  [M,ceil(K/64),2] E8M0 bytes
+ *   group_list      [E] int64 (type per problem.group_list_type); checked on the device
+ *   logit           [M] float32, or NULL for weight 1 (has_logit = False)
+ *   row_index       [M] int64 or int32; values in [0,batch), checked on the device
+ *   shared_input    [shared_rows,N] bfloat16, or NULL when shared_rows == 0
+ *   out             [batch,N] float32, read and accumulated into in place
+ *   prepared        output of gmmfr_prepare_weights for the same x2/scale, or NULL
+ *   workspace       at least gmmfr_workspace_size bytes, 256-byte aligned; its
+ *                   contents on entry do not matter; it must not be shared by two
+ *                   calls in flight at the same time
+ * Without GMMFR_DETERMINISTIC the row scatter uses float atomics, so the FP32
+ * rounding order, and the low bits of `out`, can differ run to run (the aclnn
+ * operator is non-deterministic by default, "确定性计算").  With it, every out
+ * element is  ((out + c_t1) + c_t2) + ... + shared  over its tokens in
+ * ascending order, and results are bit-identical run to run on one device.
+ * Device-side index errors do not fail the call: they set bits of the device
+ * error word, read with gmmfr_check_device_errors.
+ */
+GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing(
+    const gmmfr_problem* problem, const void* x1, const void* x2, const void* scale,
+    const void* pertoken_scale, const int64_t* group_list, const float* logit,
+    const void* row_index, const void* shared_input, float* out, const void* prepared,
+    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * SYNCHRONISES `stream`, then reads the device error word that the last call
+ * using `workspace` left there (GMMFR_DEV_* bits, 0 when clean) into *bits.
+ * Returns GMMFR_ERR_DEVICE when any bit is set, GMMFR_OK otherwise.
+ */
+GMMFR_API gmmfr_status gmmfr_check_device_errors(const void* workspace, void* stream, uint32_t* bits);
+
+/* Message of the last error returned on the calling thread ("" if none). */
+GMMFR_API const char* gmmfr_last_error(void);
+
+/*
+ * Kernel timing for measurement.  gmmfr_profile_begin(n) creates CUDA events
+ * for up to n calls; each later call records events around each of its
+ * kernels on its stream.  gmmfr_profile_end SYNCHRONISES the device, writes
+ * ms[call * GMMFR_PROFILE_SLOTS + slot] (-1 where a slot's kernel did not run),
+ * sets *n_calls, and stops recording.
+ * Slots: 0 weight preparation inside the call, 1 prologue (group ranges and
+ * token-scale layout), 2 grouped GEMM with fused epilogue, 3 deterministic combine.
+ */
+#define GMMFR_PROFILE_SLOTS 4
+GMMFR_API gmmfr_status gmmfr_profile_begin(int max_calls);
+GMMFR_API gmmfr_status gmmfr_profile_end(float* ms, int max_entries, int* n_calls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GMMFR_H */

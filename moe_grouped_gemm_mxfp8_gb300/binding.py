@@ -1,0 +1,202 @@
+"""ctypes binding of the gmmfr C ABI (include/gmmfr.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  The functions named like the C entry points take raw device
+addresses (int) or None; :func:`tensor_args` and :func:`run` turn torch
+tensors into those.  The library is loaded on first use; if it has not been
+built, loading raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libgmmfr.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = range(6)
+E4M3, E5M2 = 0, 1
+INDEX_I64, INDEX_I32 = 0, 1
+DETERMINISTIC = 1
+DEV_BAD_GROUP_LIST, DEV_BAD_ROW_INDEX, DEV_TIMEOUT = 1, 2, 4
+PROFILE_SLOTS = 4
+PROFILE_SLOT_NAMES = ("prep", "prologue", "gemm", "combine")
+
+# exported entry points, as declared in include/gmmfr.h
+ENTRY_POINTS = (
+    "gmmfr_prepared_weights_size", "gmmfr_prepare_weights", "gmmfr_workspace_size",
+    "gmmfr_grouped_matmul_finalize_routing", "gmmfr_check_device_errors", "gmmfr_last_error",
+    "gmmfr_profile_begin", "gmmfr_profile_end",
+)
+
+
+class Problem(ctypes.Structure):
+    """Mirror of gmmfr_problem."""
+    _fields_ = [
+        ("M", ctypes.c_int64), ("K", ctypes.c_int64), ("N", ctypes.c_int64),
+        ("E", ctypes.c_int64), ("batch", ctypes.c_int64),
+        ("x1_format", ctypes.c_int32), ("x2_format", ctypes.c_int32),
+        ("transpose_x2", ctypes.c_int32), ("scale_per_expert", ctypes.c_int32),
+        ("group_list_type", ctypes.c_int32), ("row_index_type", ctypes.c_int32),
+        ("shared_rows", ctypes.c_int64), ("shared_offset", ctypes.c_int64),
+        ("shared_weight", ctypes.c_float), ("flags", ctypes.c_uint32),
+    ]
+
+
+class GmmfrError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"gmmfr status {status}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once).  Raises if it is missing: there is no fallback."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"gmmfr CUDA library not built ({path}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(path)
+            P = ctypes.POINTER(Problem)
+            vp, sz = ctypes.c_void_p, ctypes.c_size_t
+            lib.gmmfr_prepared_weights_size.argtypes = [P, ctypes.POINTER(sz)]
+            lib.gmmfr_prepare_weights.argtypes = [P, vp, vp, vp, sz, vp]
+            lib.gmmfr_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
+            lib.gmmfr_grouped_matmul_finalize_routing.argtypes = [P] + [vp] * 11 + [sz, vp]
+            lib.gmmfr_check_device_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+            lib.gmmfr_last_error.restype = ctypes.c_char_p
+            lib.gmmfr_profile_begin.argtypes = [ctypes.c_int]
+            lib.gmmfr_profile_end.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int,
+                                              ctypes.POINTER(ctypes.c_int)]
+            for name in ENTRY_POINTS:
+                if name != "gmmfr_last_error":
+                    getattr(lib, name).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def gmmfr_last_error() -> str:
+    return load().gmmfr_last_error().decode()
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        raise GmmfrError(status, gmmfr_last_error())
+
+
+def make_problem(*, M, K, N, E, batch, x1_format=E4M3, x2_format=E4M3, transpose_x2=False,
+                 scale_per_expert=False, group_list_type=1, row_index_type=INDEX_I64, shared_rows=0,
+                 shared_offset=0, shared_weight=1.0, deterministic=False) -> Problem:
+    return Problem(M=M, K=K, N=N, E=E, batch=batch, x1_format=x1_format, x2_format=x2_format,
+                   transpose_x2=int(bool(transpose_x2)), scale_per_expert=int(bool(scale_per_expert)),
+                   group_list_type=group_list_type, row_index_type=row_index_type,
+                   shared_rows=shared_rows, shared_offset=shared_offset, shared_weight=shared_weight,
+                   flags=DETERMINISTIC if deterministic else 0)
+
+
+def problem_from_spec(spec, deterministic: bool = False, row_index_type: int = INDEX_I64) -> Problem:
+    """gmmfr_problem for a workloads.Spec."""
+    return make_problem(M=spec.M, K=spec.K, N=spec.N, E=spec.E, batch=spec.batch, x1_format=spec.x1_dtype,
+                        x2_format=spec.x2_dtype, transpose_x2=spec.transpose_x2,
+                        scale_per_expert=spec.scale_per_expert, group_list_type=spec.group_list_type,
+                        row_index_type=row_index_type, shared_rows=spec.n_shared,
+                        shared_offset=spec.shared_offset, shared_weight=spec.shared_weight,
+                        deterministic=deterministic)
+
+
+def gmmfr_prepared_weights_size(problem: Problem) -> int:
+    n = ctypes.c_size_t()
+    _check(load().gmmfr_prepared_weights_size(ctypes.byref(problem), ctypes.byref(n)))
+    return n.value
+
+
+def gmmfr_prepare_weights(problem: Problem, x2: Optional[int], scale: Optional[int], prepared: Optional[int],
+                          prepared_bytes: int, stream: Optional[int] = None) -> None:
+    _check(load().gmmfr_prepare_weights(ctypes.byref(problem), x2, scale, prepared, prepared_bytes, stream))
+
+
+def gmmfr_workspace_size(problem: Problem, have_prepared: bool) -> int:
+    n = ctypes.c_size_t()
+    _check(load().gmmfr_workspace_size(ctypes.byref(problem), int(bool(have_prepared)), ctypes.byref(n)))
+    return n.value
+
+
+def gmmfr_grouped_matmul_finalize_routing(problem: Problem, x1, x2, scale, pertoken_scale, group_list, logit,
+                                          row_index, shared_input, out, prepared, workspace, workspace_bytes,
+                                          stream=None) -> None:
+    _check(load().gmmfr_grouped_matmul_finalize_routing(
+        ctypes.byref(problem), x1, x2, scale, pertoken_scale, group_list, logit, row_index, shared_input,
+        out, prepared, workspace, workspace_bytes, stream))
+
+
+def gmmfr_check_device_errors(workspace: int, stream: Optional[int] = None) -> int:
+    """Synchronises `stream`; returns the device error bits (0 when clean)."""
+    bits = ctypes.c_uint32()
+    st = load().gmmfr_check_device_errors(workspace, stream, ctypes.byref(bits))
+    if st not in (OK, ERR_DEVICE):
+        _check(st)
+    return bits.value
+
+
+def gmmfr_profile_begin(max_calls: int) -> None:
+    _check(load().gmmfr_profile_begin(max_calls))
+
+
+def gmmfr_profile_end(max_calls: int):
+    """Per recorded call, the kernel times in ms by slot (-1 when not run)."""
+    buf = (ctypes.c_float * (max_calls * PROFILE_SLOTS))()
+    n = ctypes.c_int()
+    _check(load().gmmfr_profile_end(buf, len(buf), ctypes.byref(n)))
+    return [[buf[c * PROFILE_SLOTS + s] for s in range(PROFILE_SLOTS)] for c in range(n.value)]
+
+
+# ---------------------------------------------------------------------------- torch marshalling
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("gmmfr takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("gmmfr takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def prepare_weights(problem: Problem, x2, scale, stream=None):
+    """Allocate (torch) and fill the prepared-weight buffer for x2/scale."""
+    import torch
+    n = gmmfr_prepared_weights_size(problem)
+    buf = torch.empty(max(n, 16), dtype=torch.uint8, device=x2.device)
+    gmmfr_prepare_weights(problem, _ptr(x2), _ptr(scale), _ptr(buf), n, _stream(stream))
+    return buf
+
+
+def workspace(problem: Problem, have_prepared: bool, device) -> "torch.Tensor":
+    import torch
+    n = gmmfr_workspace_size(problem, have_prepared)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def run(problem: Problem, inputs: dict, out, prepared=None, ws=None, stream=None) -> None:
+    """One call of the operator on device tensors (``inputs`` as made by
+    workloads.make_inputs); accumulates into ``out`` in place."""
+    if ws is None:
+        ws = workspace(problem, prepared is not None, out.device)
+    gmmfr_grouped_matmul_finalize_routing(
+        problem, _ptr(inputs["x1"]), _ptr(inputs["x2"]) if prepared is None else None,
+        _ptr(inputs["scale"]) if prepared is None else None, _ptr(inputs["pertoken_scale"]),
+        _ptr(inputs["group_list"]), _ptr(inputs.get("logit")), _ptr(inputs["row_index"]),
+        _ptr(inputs.get("shared_input")), _ptr(out), _ptr(prepared), _ptr(ws), ws.numel(), _stream(stream))
+    return ws

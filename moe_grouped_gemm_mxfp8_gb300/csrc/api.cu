@@ -1,0 +1,422 @@
+// C ABI of the MXFP8 grouped-matmul-finalize-routing library (declared in
+// include/gmmfr.h): argument checks, workspace layout, tensor map of x1, and the
+// launch sequence prologue -> grouped GEMM -> (deterministic) combine.
+#include "gmmfr.h"
+
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gmmfr_status fail(gmmfr_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+gmmfr_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GMMFR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int64_t kMaxExperts = 1024;
+constexpr int kSplitRefSms = 152;  // fixes the deterministic split independently of the device
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+gmmfr_status validate(const gmmfr_problem* p) {
+  if (!p) return fail(GMMFR_ERR_INVALID_ARG, "problem is NULL");
+  if (p->M < 0 || p->M >= (int64_t(1) << 31)) return fail(GMMFR_ERR_INVALID_ARG, "M=%lld out of range [0, 2^31)", (long long)p->M);
+  if (p->K < 1 || p->K >= (int64_t(1) << 31)) return fail(GMMFR_ERR_INVALID_ARG, "K=%lld out of range [1, 2^31)", (long long)p->K);
+  if (p->N < 0 || p->N >= (int64_t(1) << 31)) return fail(GMMFR_ERR_INVALID_ARG, "N=%lld out of range [0, 2^31)", (long long)p->N);
+  if (p->E < 1 || p->E > kMaxExperts) return fail(GMMFR_ERR_INVALID_ARG, "E=%lld out of range [1, 1024]", (long long)p->E);
+  if (p->batch < 0 || p->batch >= (int64_t(1) << 31)) return fail(GMMFR_ERR_INVALID_ARG, "batch=%lld out of range [0, 2^31)", (long long)p->batch);
+  if (p->x1_format != GMMFR_E4M3 && p->x1_format != GMMFR_E5M2) return fail(GMMFR_ERR_INVALID_ARG, "x1_format=%d is not E4M3 (0) or E5M2 (1)", p->x1_format);
+  if (p->x2_format != GMMFR_E4M3 && p->x2_format != GMMFR_E5M2) return fail(GMMFR_ERR_INVALID_ARG, "x2_format=%d is not E4M3 (0) or E5M2 (1)", p->x2_format);
+  if (p->transpose_x2 != 0 && p->transpose_x2 != 1) return fail(GMMFR_ERR_INVALID_ARG, "transpose_x2 must be 0 or 1");
+  if (p->scale_per_expert != 0 && p->scale_per_expert != 1) return fail(GMMFR_ERR_INVALID_ARG, "scale_per_expert must be 0 or 1");
+  if (p->group_list_type != 0 && p->group_list_type != 1) return fail(GMMFR_ERR_INVALID_ARG, "group_list_type=%d is not 0 (prefix sums) or 1 (counts)", p->group_list_type);
+  if (p->row_index_type != GMMFR_INDEX_I64 && p->row_index_type != GMMFR_INDEX_I32) return fail(GMMFR_ERR_INVALID_ARG, "row_index_type=%d is not 0 (int64) or 1 (int32)", p->row_index_type);
+  if (p->shared_rows < 0) return fail(GMMFR_ERR_INVALID_ARG, "shared_rows=%lld is negative", (long long)p->shared_rows);
+  if (p->shared_offset < 0) return fail(GMMFR_ERR_INVALID_ARG, "shared_offset=%lld is negative", (long long)p->shared_offset);
+  if (p->shared_offset + p->shared_rows > p->batch)
+    return fail(GMMFR_ERR_INVALID_ARG, "shared_offset + shared_rows = %lld exceeds batch = %lld",
+                (long long)(p->shared_offset + p->shared_rows), (long long)p->batch);
+  if (p->flags & ~GMMFR_DETERMINISTIC) return fail(GMMFR_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
+  if (p->K % 16 != 0) return fail(GMMFR_ERR_UNSUPPORTED, "K=%lld: this build needs K %% 16 == 0 (x1 rows are moved by TMA)", (long long)p->K);
+  return GMMFR_OK;
+}
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kSplitRefSms;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return kSplitRefSms;
+  return sms;
+}
+
+int choose_tmax(const gmmfr_problem* p) {
+  if (const char* s = std::getenv("GMMFR_TMAX")) {
+    const int v = std::atoi(s);
+    if (v == 32 || v == 64 || v == 128) return v;
+  }
+  const int64_t avg = cdiv(p->M, p->E);
+  return avg <= 32 ? 64 : 128;
+}
+
+struct Layout {
+  int64_t NT, KB, Ks;
+  int tmax, split;
+  int64_t max_groups;
+  size_t off_groups, off_tsf, off_cnt, off_rowptr, off_cursor, off_sorted, off_y, off_prep, total;
+};
+
+Layout make_layout(const gmmfr_problem* p, bool have_prepared) {
+  Layout L{};
+  L.NT = cdiv(p->N, gmmfr::kTileN);
+  L.KB = cdiv(p->K, gmmfr::kTileK);
+  L.Ks = cdiv(p->K, 64);
+  L.tmax = choose_tmax(p);
+  L.max_groups = p->E + cdiv(p->M, L.tmax);
+  const bool det = p->flags & GMMFR_DETERMINISTIC;
+  if (det) {
+    const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(p->E, std::max<int64_t>(p->M, 1)) * L.NT);
+    L.split = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(8, L.KB), cdiv(4 * kSplitRefSms, tiles)));
+  } else {
+    L.split = 1;
+  }
+  size_t off = gmmfr::kHdrBytes;
+  L.off_groups = off;
+  off = align256(off + sizeof(int4) * (size_t)L.max_groups);
+  L.off_tsf = off;
+  off = align256(off + (size_t)L.max_groups * L.KB * gmmfr::kSfChunk);
+  if (det) {
+    L.off_cnt = off;
+    off = align256(off + sizeof(int32_t) * (size_t)p->batch);
+    L.off_rowptr = off;
+    off = align256(off + sizeof(int32_t) * (size_t)(p->batch + 1));
+    L.off_cursor = off;
+    off = align256(off + sizeof(int32_t) * (size_t)p->batch);
+    L.off_sorted = off;
+    off = align256(off + sizeof(int32_t) * (size_t)p->M);
+    L.off_y = off;
+    off = align256(off + sizeof(float) * (size_t)L.split * p->M * p->N);
+  }
+  if (!have_prepared) {
+    L.off_prep = off;
+    off = align256(off + (size_t)p->E * L.NT * L.KB * gmmfr::kPrepTileBytes);
+  }
+  L.total = off;
+  return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// ---------------------------------------------------------------- kernel timing
+struct Profiler {
+  std::mutex mu;
+  bool active = false;
+  int max_calls = 0, n_calls = 0;
+  std::vector<cudaEvent_t> ev;  // [call][slot][begin,end]
+  std::vector<char> used;       // [call][slot]
+} g_prof;
+
+struct CallTimer {
+  int call = -1;
+  CallTimer() {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (g_prof.active && g_prof.n_calls < g_prof.max_calls) call = g_prof.n_calls++;
+  }
+  void begin(int slot, cudaStream_t s) {
+    if (call >= 0) cudaEventRecord(g_prof.ev[(call * GMMFR_PROFILE_SLOTS + slot) * 2], s);
+  }
+  void end(int slot, cudaStream_t s) {
+    if (call >= 0) {
+      cudaEventRecord(g_prof.ev[(call * GMMFR_PROFILE_SLOTS + slot) * 2 + 1], s);
+      g_prof.used[call * GMMFR_PROFILE_SLOTS + slot] = 1;
+    }
+  }
+};
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* gmmfr_last_error(void) { return g_last_error.c_str(); }
+
+gmmfr_status gmmfr_prepared_weights_size(const gmmfr_problem* problem, size_t* bytes) {
+  if (gmmfr_status st = validate(problem)) return st;
+  if (!bytes) return fail(GMMFR_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = (size_t)problem->E * cdiv(problem->N, gmmfr::kTileN) * cdiv(problem->K, gmmfr::kTileK) * gmmfr::kPrepTileBytes;
+  return GMMFR_OK;
+}
+
+gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int have_prepared, size_t* bytes) {
+  if (gmmfr_status st = validate(problem)) return st;
+  if (!bytes) return fail(GMMFR_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = make_layout(problem, have_prepared != 0).total;
+  return GMMFR_OK;
+}
+
+static gmmfr::PrepParams prep_params(const gmmfr_problem* p, const void* x2, const void* scale, void* dst) {
+  gmmfr::PrepParams pp{};
+  pp.x2 = static_cast<const uint8_t*>(x2);
+  pp.scale = static_cast<const uint8_t*>(scale);
+  pp.prepared = static_cast<uint8_t*>(dst);
+  pp.E = p->E;
+  pp.K = p->K;
+  pp.N = p->N;
+  pp.NT = (int32_t)cdiv(p->N, gmmfr::kTileN);
+  pp.KB = (int32_t)cdiv(p->K, gmmfr::kTileK);
+  pp.Ks = (int32_t)cdiv(p->K, 64);
+  pp.transpose_x2 = p->transpose_x2;
+  pp.scale_per_expert = p->scale_per_expert;
+  return pp;
+}
+
+gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const void* x2, const void* scale, void* prepared,
+                                   size_t prepared_bytes, void* stream) {
+  if (gmmfr_status st = validate(problem)) return st;
+  size_t need = 0;
+  gmmfr_prepared_weights_size(problem, &need);
+  if (problem->N == 0) return GMMFR_OK;
+  if (!x2 || !scale) return fail(GMMFR_ERR_INVALID_ARG, "x2 and scale must be non-NULL");
+  if (!prepared) return fail(GMMFR_ERR_INVALID_ARG, "prepared is NULL");
+  if (prepared_bytes < need) return fail(GMMFR_ERR_WORKSPACE, "prepared buffer has %zu bytes, needs %zu", prepared_bytes, need);
+  if (!aligned(prepared, 16)) return fail(GMMFR_ERR_WORKSPACE, "prepared buffer must be 16-byte aligned");
+  cudaError_t e = gmmfr::launch_prep(prep_params(problem, x2, scale, prepared), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "weight preparation launch");
+  return GMMFR_OK;
+}
+
+gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem, const void* x1, const void* x2,
+                                                   const void* scale, const void* pertoken_scale,
+                                                   const int64_t* group_list, const float* logit,
+                                                   const void* row_index, const void* shared_input, float* out,
+                                                   const void* prepared, void* workspace, size_t workspace_bytes,
+                                                   void* stream) {
+  if (gmmfr_status st = validate(problem)) return st;
+  const gmmfr_problem& p = *problem;
+  const bool det = p.flags & GMMFR_DETERMINISTIC;
+  if (p.N == 0 || p.batch == 0 && p.M == 0) return GMMFR_OK;  // nothing to compute
+  if (p.M > 0 && (!x1 || !pertoken_scale || !row_index))
+    return fail(GMMFR_ERR_INVALID_ARG, "x1, pertoken_scale and row_index must be non-NULL when M > 0");
+  if (!group_list) return fail(GMMFR_ERR_INVALID_ARG, "group_list is NULL");
+  if (p.batch > 0 && !out) return fail(GMMFR_ERR_INVALID_ARG, "out is NULL");
+  if (p.shared_rows > 0 && !shared_input) return fail(GMMFR_ERR_INVALID_ARG, "shared_input is NULL but shared_rows > 0");
+  if (!prepared && (!x2 || !scale)) return fail(GMMFR_ERR_INVALID_ARG, "either prepared or both x2 and scale must be given");
+  if (x1 && !aligned(x1, 16)) return fail(GMMFR_ERR_INVALID_ARG, "x1 must be 16-byte aligned");
+  if (prepared && !aligned(prepared, 16)) return fail(GMMFR_ERR_INVALID_ARG, "prepared must be 16-byte aligned");
+  if (!aligned(group_list, 8) || (row_index && !aligned(row_index, p.row_index_type == GMMFR_INDEX_I32 ? 4 : 8)) ||
+      (logit && !aligned(logit, 4)) || (out && !aligned(out, 4)) || (shared_input && !aligned(shared_input, 2)))
+    return fail(GMMFR_ERR_INVALID_ARG, "an input is not aligned to its element size");
+  const Layout L = make_layout(problem, prepared != nullptr);
+  if (!workspace) return fail(GMMFR_ERR_WORKSPACE, "workspace is NULL (needs %zu bytes)", L.total);
+  if (workspace_bytes < L.total) return fail(GMMFR_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
+  if (!aligned(workspace, 256)) return fail(GMMFR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+  if (!encode) return fail(GMMFR_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* hdr = reinterpret_cast<uint32_t*>(ws);
+  const int sms = device_sms();
+  CallTimer timer;
+  cudaError_t e;
+
+  const uint8_t* wprep = static_cast<const uint8_t*>(prepared);
+  if (!prepared) {
+    timer.begin(0, s);
+    e = gmmfr::launch_prep(prep_params(problem, x2, scale, ws + L.off_prep), s);
+    timer.end(0, s);
+    if (e != cudaSuccess) return cuda_fail(e, "weight preparation launch");
+    wprep = ws + L.off_prep;
+  }
+
+  // x1 [M, K] bytes as a 2-D tensor, 16-row x 128-byte boxes, 128-byte swizzle
+  CUtensorMap tmap;
+  {
+    const bool empty = p.M == 0;
+    cuuint64_t dims[2] = {(cuuint64_t)(empty ? 16 : p.K), (cuuint64_t)(empty ? 1 : p.M)};
+    cuuint64_t strides[1] = {(cuuint64_t)(empty ? 16 : p.K)};
+    cuuint32_t box[2] = {(cuuint32_t)gmmfr::kTileK, (cuuint32_t)gmmfr::kTokBox};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, empty ? (void*)ws : const_cast<void*>(x1), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GMMFR_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  }
+
+  gmmfr::PrologueParams pp{};
+  pp.group_list = group_list;
+  pp.pertoken_scale = static_cast<const uint8_t*>(pertoken_scale);
+  pp.row_index = row_index;
+  pp.hdr = hdr;
+  pp.groups = reinterpret_cast<int4*>(ws + L.off_groups);
+  pp.tsf = ws + L.off_tsf;
+  if (det) {
+    pp.cnt = reinterpret_cast<int32_t*>(ws + L.off_cnt);
+    pp.row_ptr = reinterpret_cast<int32_t*>(ws + L.off_rowptr);
+    pp.cursor = reinterpret_cast<int32_t*>(ws + L.off_cursor);
+    pp.sorted = reinterpret_cast<int32_t*>(ws + L.off_sorted);
+  }
+  pp.M = p.M;
+  pp.K = p.K;
+  pp.batch = p.batch;
+  pp.E = (int32_t)p.E;
+  pp.KB = (int32_t)L.KB;
+  pp.Ks = (int32_t)L.Ks;
+  pp.tmax = L.tmax;
+  pp.group_list_type = p.group_list_type;
+  pp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;
+  pp.deterministic = det;
+  const int64_t sf_items = L.max_groups * L.KB;
+  const int pro_grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, cdiv(sf_items, 8)));
+  timer.begin(1, s);
+  e = gmmfr::launch_prologue(pp, pro_grid, s);
+  timer.end(1, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
+
+  gmmfr::GemmParams gp{};
+  gp.prepared = wprep;
+  gp.tsf = ws + L.off_tsf;
+  gp.groups = reinterpret_cast<const int4*>(ws + L.off_groups);
+  gp.hdr = hdr;
+  gp.logit = logit;
+  gp.row_index = row_index;
+  gp.shared = static_cast<const uint16_t*>(shared_input);
+  gp.out = out;
+  gp.ybuf = det ? reinterpret_cast<float*>(ws + L.off_y) : nullptr;
+  gp.err = hdr + gmmfr::kHdrErr;
+  gp.M = p.M;
+  gp.N = p.N;
+  gp.K = p.K;
+  gp.batch = p.batch;
+  gp.shared_rows = shared_input ? p.shared_rows : 0;
+  gp.shared_offset = p.shared_offset;
+  gp.shared_weight = p.shared_weight;
+  gp.NT = (int32_t)L.NT;
+  gp.KB = (int32_t)L.KB;
+  gp.split = L.split;
+  gp.deterministic = det;
+  gp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;
+  // instruction descriptor: A = weights (x2 format), B = tokens (x1 format),
+  // E8M0 scales (bit 23), M = 128 (bits 24..28 hold M >> 4)
+  gp.idesc = (1u << 23) | ((uint32_t)p.x2_format << 7) | ((uint32_t)p.x1_format << 10) | ((128u >> 4) << 24);
+  gp.timeout_ns = 4000000000ll;
+  gp.test_stall = 0;
+  if (const char* t = std::getenv("GMMFR_TEST_STALL_NS")) {  // testing aid: bounded-wait timeout path
+    gp.test_stall = 1;
+    gp.timeout_ns = std::atoll(t) > 0 ? std::atoll(t) : 1000000;
+  }
+  timer.begin(2, s);
+  e = gmmfr::launch_gemm(tmap, gp, L.tmax, sms, s);
+  timer.end(2, s);
+  if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
+
+  if (det) {
+    gmmfr::CombineParams cp{};
+    cp.hdr = hdr;
+    cp.row_ptr = pp.row_ptr;
+    cp.sorted = pp.sorted;
+    cp.ybuf = gp.ybuf;
+    cp.shared = gp.shared;
+    cp.out = out;
+    cp.M = p.M;
+    cp.N = p.N;
+    cp.batch = p.batch;
+    cp.shared_rows = gp.shared_rows;
+    cp.shared_offset = p.shared_offset;
+    cp.shared_weight = p.shared_weight;
+    cp.split = L.split;
+    timer.begin(3, s);
+    e = gmmfr::launch_combine(cp, s);
+    timer.end(3, s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
+  return GMMFR_OK;
+}
+
+gmmfr_status gmmfr_check_device_errors(const void* workspace, void* stream, uint32_t* bits) {
+  if (!workspace || !bits) return fail(GMMFR_ERR_INVALID_ARG, "workspace and bits must be non-NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *bits = v;
+  if (v) return fail(GMMFR_ERR_DEVICE, "device error bits 0x%x", v);
+  return GMMFR_OK;
+}
+
+gmmfr_status gmmfr_profile_begin(int max_calls) {
+  if (max_calls < 1) return fail(GMMFR_ERR_INVALID_ARG, "max_calls must be >= 1");
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (g_prof.active) return fail(GMMFR_ERR_INVALID_ARG, "profiling already active");
+  g_prof.ev.assign((size_t)max_calls * GMMFR_PROFILE_SLOTS * 2, nullptr);
+  for (auto& ev : g_prof.ev) {
+    cudaError_t e = cudaEventCreate(&ev);
+    if (e != cudaSuccess) {
+      for (auto& x : g_prof.ev)
+        if (x) cudaEventDestroy(x);
+      g_prof.ev.clear();
+      return cuda_fail(e, "cudaEventCreate");
+    }
+  }
+  g_prof.used.assign((size_t)max_calls * GMMFR_PROFILE_SLOTS, 0);
+  g_prof.max_calls = max_calls;
+  g_prof.n_calls = 0;
+  g_prof.active = true;
+  return GMMFR_OK;
+}
+
+gmmfr_status gmmfr_profile_end(float* ms, int max_entries, int* n_calls) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.active) return fail(GMMFR_ERR_INVALID_ARG, "profiling not active");
+  g_prof.active = false;
+  cudaError_t e = cudaDeviceSynchronize();
+  gmmfr_status st = GMMFR_OK;
+  if (e != cudaSuccess) st = cuda_fail(e, "cudaDeviceSynchronize");
+  const int n = g_prof.n_calls;
+  if (n_calls) *n_calls = n;
+  for (int c = 0; c < n && st == GMMFR_OK; ++c)
+    for (int sl = 0; sl < GMMFR_PROFILE_SLOTS; ++sl) {
+      const int idx = c * GMMFR_PROFILE_SLOTS + sl;
+      if (!ms || idx >= max_entries) continue;
+      float v = -1.f;
+      if (g_prof.used[idx] && cudaEventElapsedTime(&v, g_prof.ev[idx * 2], g_prof.ev[idx * 2 + 1]) != cudaSuccess) v = -1.f;
+      ms[idx] = v;
+    }
+  for (auto& x : g_prof.ev) cudaEventDestroy(x);
+  g_prof.ev.clear();
+  g_prof.used.clear();
+  return st;
+}
+
+}  // extern "C"

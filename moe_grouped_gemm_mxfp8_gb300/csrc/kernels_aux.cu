@@ -1,0 +1,318 @@
+// Auxiliary kernels of MXFP8 grouped-matmul-finalize-routing:
+//   - weight preparation (one-time re-layout of x2 and its scales into GEMM tiles),
+//   - per-call prologue (group_list decode and checks, token groups, token-scale
+//     layout for the tensor cores, and the row CSR of the deterministic mode),
+//   - deterministic combine (row-ordered sum of the per-token results).
+#include "common.cuh"
+
+namespace gmmfr {
+
+// ============================================================================ weight prep
+// Prepared tile (e, j, kb): 128 output columns n = j*128 + r by 128 K bytes
+// k = kb*128 + c, stored as the shared-memory image of a K-major operand with
+// the 128-byte swizzle (16-byte chunk c/16 of row r lands at chunk (c/16)^(r%8)),
+// then 512 scale bytes: scale of (row r, 32-block q) at 16*(r%32) + 4*(r/32) + q,
+// the 32-row x 16-byte block that tcgen05.cp ... 32x128b.warpx4 spreads over the
+// four TMEM lane quadrants.  Columns n >= N and K bytes k >= K are zero; their
+// scales (and scales of 32-blocks starting at or past K) are 127 (= 1.0).
+__global__ void __launch_bounds__(256) prep_kernel(PrepParams p) {
+  const int64_t tiles = p.E * p.NT * p.KB;
+  const int64_t Ks = p.Ks;
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t kb = tile % p.KB;
+    const int64_t j = (tile / p.KB) % p.NT;
+    const int64_t e = tile / ((int64_t)p.KB * p.NT);
+    uint8_t* dst = p.prepared + tile * kPrepTileBytes;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int id = threadIdx.x + it * 256;
+      const int r = id & 127, c = id >> 7;  // warp = 32 consecutive rows of one chunk column
+      const int64_t n = j * kTileN + r;
+      const int64_t k0 = kb * kTileK + c * 16;
+      uint8_t b[16];
+      if (p.transpose_x2) {  // x2 [E, N, K]: the 16 bytes are contiguous
+        const uint8_t* src = p.x2 + (e * p.N + n) * p.K + k0;
+        if (n < p.N && k0 + 16 <= p.K && ((reinterpret_cast<uintptr_t>(src) & 15) == 0)) {
+          *reinterpret_cast<uint4*>(b) = *reinterpret_cast<const uint4*>(src);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) b[i] = (n < p.N && k0 + i < p.K) ? src[i] : 0;
+        }
+      } else {  // x2 [E, K, N]: one byte per K row; a warp reads 32 consecutive n of a row
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          b[i] = (n < p.N && k0 + i < p.K) ? p.x2[(e * p.K + k0 + i) * p.N + n] : 0;
+      }
+      *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = *reinterpret_cast<const uint4*>(b);
+    }
+    const int64_t sbase = p.scale_per_expert ? e * Ks * p.N * 2 : 0;
+    for (int id = threadIdx.x; id < kSfChunk; id += 256) {
+      const int r = id & 127, q = id >> 7;
+      const int64_t n = j * kTileN + r;
+      const int64_t g = kb * 4 + q;  // 32-element block index along K
+      uint8_t v = 127;
+      if (n < p.N && g * 32 < p.K) {
+        const int64_t kp = g >> 1, h = g & 1;
+        v = p.transpose_x2 ? p.scale[sbase + (n * Ks + kp) * 2 + h] : p.scale[sbase + (kp * p.N + n) * 2 + h];
+      }
+      dst[kWTileBytes + 16 * (r & 31) + 4 * (r >> 5) + q] = v;
+    }
+  }
+}
+
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
+  const int64_t tiles = p.E * p.NT * p.KB;
+  if (tiles == 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t grid = tiles < (int64_t)sms * 8 ? tiles : (int64_t)sms * 8;
+  prep_kernel<<<(unsigned)grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ============================================================================ prologue
+// Block-wide inclusive scan over 1024 threads (sum or max) of int64 values.
+// `total` receives the scan's last value.
+template <bool kMax>
+__device__ int64_t block_scan_incl(int64_t v, int64_t* s_warp, int64_t* total = nullptr) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = kMax ? (u > v ? u : v) : v + u;
+  }
+  if (lane == 31) s_warp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w = kMax ? (u > w ? u : w) : w + u;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  if (warp > 0) {
+    const int64_t u = s_warp[warp - 1];
+    v = kMax ? (u > v ? u : v) : v + u;
+  }
+  if (total) *total = s_warp[31];
+  __syncthreads();
+  return v;
+}
+
+__device__ __forceinline__ int64_t load_row(const void* rows, int row_i32, int64_t t) {
+  return row_i32 ? (int64_t) static_cast<const int32_t*>(rows)[t] : static_cast<const int64_t*>(rows)[t];
+}
+
+// Every block decodes the (at most 1024) expert ranges itself; block 0 also
+// publishes the group table and header; all blocks then lay out token scales;
+// in deterministic mode the last block builds the row CSR.
+__global__ void __launch_bounds__(1024) prologue_kernel(PrologueParams p) {
+  __shared__ int64_t s_warp[32];
+  __shared__ int64_t s_start[1024];
+  __shared__ int64_t s_end[1024];
+  __shared__ int32_t s_gbase[1025];
+  __shared__ uint32_t s_err;
+  const int tid = threadIdx.x;
+  const int E = p.E;
+  const int64_t M = p.M;
+  if (tid == 0) s_err = 0;
+  __syncthreads();
+
+  // ---- expert ranges (contiguous, clamped to [0, M]; section 4.3 group_list formats)
+  const int64_t g = tid < E ? p.group_list[tid] : 0;
+  int64_t end;
+  if (p.group_list_type == 1) {
+    // counts: end_e = min(sum_{i<=e} max(g_i,0), M); saturate each term at M+1
+    const int64_t c = tid < E ? (g < 0 ? 0 : (g > M ? M + 1 : g)) : 0;
+    if (tid < E && g < 0) atomicOr(&s_err, kErrBadGroupList);
+    const int64_t incl = block_scan_incl<false>(c, s_warp);
+    if (tid == E - 1 && incl > M) atomicOr(&s_err, kErrBadGroupList);
+    end = incl < M ? incl : M;
+  } else {
+    // prefix sums: end_e = min(max(0, g_0..g_e), M)
+    const int64_t prev = (tid > 0 && tid < E) ? p.group_list[tid - 1] : 0;
+    if (tid < E && (g < prev || g > M)) atomicOr(&s_err, kErrBadGroupList);
+    const int64_t c = tid < E ? (g < 0 ? 0 : (g > M ? M : g)) : 0;
+    const int64_t incl = block_scan_incl<true>(c, s_warp);
+    end = incl < M ? incl : M;
+  }
+  s_end[tid] = end;
+  __syncthreads();
+  const int64_t start = tid == 0 ? 0 : s_end[tid - 1];
+  s_start[tid] = start;
+  const int64_t cnt = tid < E ? end - start : 0;
+  const int64_t ng = (cnt + p.tmax - 1) / p.tmax;
+  const int64_t gincl = block_scan_incl<false>(ng, s_warp);
+  s_gbase[tid + 1] = (int32_t)gincl;
+  if (tid == 0) s_gbase[0] = 0;
+  __syncthreads();
+  const int n_groups = s_gbase[E];
+  const int64_t covered = s_end[E - 1];
+
+  if (blockIdx.x == 0) {
+    if (tid < E) {
+      const int gb = s_gbase[tid];
+      for (int i = 0; i < ng; ++i) {
+        const int64_t rem = cnt - (int64_t)i * p.tmax;
+        p.groups[gb + i] = make_int4(tid, (int)(start + (int64_t)i * p.tmax), (int)(rem < p.tmax ? rem : p.tmax), 0);
+      }
+    }
+    if (tid == 0) {
+      p.hdr[kHdrErr] = s_err;
+      p.hdr[kHdrGroups] = (uint32_t)n_groups;
+      p.hdr[kHdrCovered] = (uint32_t)covered;
+    }
+  }
+
+  // ---- token scales: per (group, K-block) a 512-byte chunk in the TMEM-copy layout
+  {
+    const int sub = tid >> 7, i = tid & 127;  // 8 chunks per block iteration, 128 threads each
+    const int64_t items = (int64_t)n_groups * p.KB;
+    const int64_t rowb = 2 * (int64_t)p.Ks;  // bytes per token row of pertoken_scale
+    for (int64_t item = (int64_t)blockIdx.x * 8 + sub; item < items; item += (int64_t)gridDim.x * 8) {
+      const int gidx = (int)(item / p.KB);
+      const int kb = (int)(item % p.KB);
+      int lo = 0, hi = E - 1;  // expert e with s_gbase[e] <= gidx < s_gbase[e+1]
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_gbase[mid] <= gidx) lo = mid; else hi = mid - 1;
+      }
+      const int64_t first = s_start[lo] + (int64_t)(gidx - s_gbase[lo]) * p.tmax;
+      const int64_t rem = (s_end[lo] - s_start[lo]) - (int64_t)(gidx - s_gbase[lo]) * p.tmax;
+      const int64_t T = rem < p.tmax ? rem : p.tmax;
+      uint32_t w = 0x7F7F7F7Fu;
+      if (i < T) {
+        const uint8_t* src = p.pertoken_scale + (first + i) * rowb;
+        w = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t blk = (int64_t)kb * 4 + q;
+          const uint32_t v = (blk * 32 < p.K) ? src[blk] : 127u;
+          w |= v << (8 * q);
+        }
+      }
+      uint8_t* dst = p.tsf + item * kSfChunk;
+      *reinterpret_cast<uint32_t*>(dst + 16 * (i & 31) + 4 * (i >> 5)) = w;
+    }
+  }
+
+  // ---- deterministic mode: CSR of covered tokens by output row (unordered within a row)
+  if (p.deterministic && blockIdx.x == gridDim.x - 1) {
+    for (int64_t r = tid; r < p.batch; r += blockDim.x) p.cnt[r] = 0;
+    __syncthreads();
+    for (int64_t t = tid; t < covered; t += blockDim.x) {
+      const int64_t r = load_row(p.row_index, p.row_i32, t);
+      if (r >= 0 && r < p.batch) atomicAdd(&p.cnt[r], 1);
+    }
+    __syncthreads();
+    int64_t running = 0;
+    for (int64_t base = 0; base < p.batch; base += blockDim.x) {
+      const int64_t r = base + tid;
+      const int64_t c = r < p.batch ? p.cnt[r] : 0;
+      int64_t chunk_total = 0;
+      const int64_t incl = block_scan_incl<false>(c, s_warp, &chunk_total);
+      if (r < p.batch) {
+        p.row_ptr[r] = (int32_t)(running + incl - c);
+        p.cursor[r] = (int32_t)(running + incl - c);
+      }
+      running += chunk_total;
+    }
+    if (tid == 0) p.row_ptr[p.batch] = (int32_t)running;
+    __syncthreads();
+    for (int64_t t = tid; t < covered; t += blockDim.x) {
+      const int64_t r = load_row(p.row_index, p.row_i32, t);
+      if (r >= 0 && r < p.batch) p.sorted[atomicAdd(&p.cursor[r], 1)] = (int32_t)t;
+    }
+  }
+}
+
+cudaError_t launch_prologue(const PrologueParams& p, int grid, cudaStream_t s) {
+  prologue_kernel<<<grid, 1024, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ============================================================================ deterministic combine
+constexpr int kCombineThreads = 256;
+constexpr int kCombineCap = 2048;  // row segments up to this length are ordered in shared memory
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// out[r, n] = ((out[r, n] + c_t1) + c_t2) + ... + w * shared[r - offset, n], the tokens
+// t1 < t2 < ... of row r in ascending order, c_t = Y[0][t][n] + Y[1][t][n] + ...
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
+  __shared__ int32_t s_tok[kCombineCap];
+  __shared__ int32_t s_ord[kCombineCap];
+  __shared__ int32_t s_min[kCombineThreads / 32];
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int beg = p.row_ptr[r];
+  const int L = p.row_ptr[r + 1] - beg;
+  const bool in_smem = L <= kCombineCap;
+  if (in_smem) {
+    for (int i = tid; i < L; i += kCombineThreads) s_tok[i] = p.sorted[beg + i];
+    __syncthreads();
+    for (int i = tid; i < L; i += kCombineThreads) {  // rank of a token = number of smaller tokens
+      const int t = s_tok[i];
+      int rank = 0;
+      for (int j = 0; j < L; ++j) rank += s_tok[j] < t;
+      s_ord[rank] = t;
+    }
+    __syncthreads();
+  }
+  const int64_t n0 = ((int64_t)blockIdx.y * kCombineThreads + tid) * 4;
+  float acc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) acc[c] = (n0 + c < p.N) ? p.out[r * p.N + n0 + c] : 0.f;
+  int prev = -1;
+  for (int i = 0; i < L; ++i) {
+    int t;
+    if (in_smem) {
+      t = s_ord[i];
+    } else {  // long segment: select the next larger token with a block-wide minimum
+      int m = 0x7fffffff;
+      for (int j = tid; j < L; j += kCombineThreads) {
+        const int u = p.sorted[beg + j];
+        if (u > prev && u < m) m = u;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if ((tid & 31) == 0) s_min[tid >> 5] = m;
+      __syncthreads();
+      m = s_min[0];
+      for (int w = 1; w < kCombineThreads / 32; ++w) m = min(m, s_min[w]);
+      __syncthreads();
+      t = m;
+      prev = m;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (n0 + c < p.N) {
+        float v = p.ybuf[(int64_t)t * p.N + n0 + c];
+        for (int s = 1; s < p.split; ++s) v += p.ybuf[((int64_t)s * p.M + t) * p.N + n0 + c];
+        acc[c] += v;
+      }
+    }
+  }
+  if (p.shared && r >= p.shared_offset && r < p.shared_offset + p.shared_rows) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (n0 + c < p.N) acc[c] += p.shared_weight * bf16_to_f32(p.shared[(r - p.shared_offset) * p.N + n0 + c]);
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    if (n0 + c < p.N) p.out[r * p.N + n0 + c] = acc[c];
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
+  if (p.batch == 0 || p.N == 0) return cudaSuccess;
+  const int64_t cols = (p.N + 4 * kCombineThreads - 1) / (4 * kCombineThreads);
+  dim3 grid((unsigned)p.batch, (unsigned)cols);
+  combine_kernel<<<grid, kCombineThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gmmfr

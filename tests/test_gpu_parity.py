@@ -1,0 +1,300 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Tolerance (per element): |gpu - oracle| <= 1e-4 * absb + 1e-6 + 2^-20 (|out_init| +
+|w * shared|), absb = sum over the element's tokens of |logit| * sum_k |a_k b_k|;
+NaN positions must match exactly; device error bits must equal the oracle's flags.
+"""
+import dataclasses
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_gemm_mxfp8_gb300 import binding as B
+from moe_grouped_gemm_mxfp8_gb300 import build as build_mod
+from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build_mod.build()
+    oracle.build()
+    B.load()
+
+
+def _dev(inp, row_i32=False):
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    if row_i32:
+        d["row_index"] = d["row_index"].to(torch.int32)
+    return d
+
+
+def gpu_run(spec, inp, deterministic=False, prepared=True, row_i32=False, d=None):
+    d = d or _dev(inp, row_i32)
+    prob = B.problem_from_spec(spec, deterministic, B.INDEX_I32 if row_i32 else B.INDEX_I64)
+    prep = B.prepare_weights(prob, d["x2"], d["scale"]) if prepared else None
+    out = d["out"].clone()
+    ws = B.run(prob, d, out, prepared=prep)
+    bits = B.gmmfr_check_device_errors(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    return out.cpu().numpy().astype(np.float64), bits
+
+
+def _extra_terms(spec, inp):
+    init = inp["out"].numpy().astype(np.float64)
+    sh = np.zeros_like(init)
+    if inp["shared_input"] is not None:
+        R = inp["shared_input"].shape[0]
+        sh[spec.shared_offset:spec.shared_offset + R] = spec.shared_weight * inp["shared_input"].to(torch.float64).numpy()
+    return init, sh
+
+
+def assert_close(got, ref, bound):
+    nan_g, nan_r = np.isnan(got), np.isnan(ref)
+    assert np.array_equal(nan_g, nan_r), f"NaN mismatch at {np.argwhere(nan_g != nan_r)[:5]}"
+    m = ~nan_r
+    err = np.abs(got[m] - ref[m])
+    ratio = err / bound[m]
+    worst = int(np.argmax(ratio)) if ratio.size else 0
+    assert ratio.size == 0 or ratio.max() <= 1.0, (
+        f"max err/bound {ratio.max():.3g} (err {err[worst]:.3g}, bound {bound[m][worst]:.3g}, ref {ref[m][worst]:.6g})")
+
+
+def check_full(spec, inp, **kw):
+    got, bits = gpu_run(spec, inp, **kw)
+    ref, absb, flags = oracle.run(oracle.problem_from_spec(spec, inp))
+    init, sh = _extra_terms(spec, inp)
+    assert_close(got, ref, oracle.tolerance(ref, absb, init, sh))
+    assert bits == flags
+    return got, ref
+
+
+def check_sampled(spec, inp, n_samples=1536, seed=0, **kw):
+    got, bits = gpu_run(spec, inp, **kw)
+    rng = np.random.default_rng(seed)
+    rows = rng.integers(0, spec.batch, n_samples)
+    cols = rng.integers(0, spec.N, n_samples)
+    # plus every row at the first and last column of the last tile
+    rows = np.concatenate([rows, np.arange(spec.batch), np.arange(spec.batch)])
+    cols = np.concatenate([cols, np.zeros(spec.batch, np.int64), np.full(spec.batch, spec.N - 1)])
+    p = oracle.problem_from_spec(spec, inp)
+    ref, absb, flags = oracle.run_sampled(p, rows, cols)
+    init, sh = _extra_terms(spec, inp)
+    bound = oracle.tolerance(ref, absb, init[rows, cols], sh[rows, cols])
+    assert_close(got[rows, cols], ref, bound)
+    assert bits == flags
+    return got
+
+
+def _spec(**kw):
+    base = dict(name="t", batch=16, M=40, K=256, N=320, E=4, seed=11)
+    base.update(kw)
+    return W.Spec(**base)
+
+
+# ----------------------------------------------------------------------------- worked example
+@pytest.mark.parametrize("transpose", [False, True])
+def test_hand_worked_example(transpose):
+    g = json.load(open(os.path.join(GOLDEN, "worked_example_mxfp8.json")))
+    M, K, N, E = g["M"], g["K"], g["N"], g["E"]
+    x1 = np.zeros((M, K), np.uint8)
+    for t, row in enumerate(g["x1_rows"]):
+        k = 0
+        for i in range(0, len(row), 2):
+            x1[t, k:k + row[i + 1]] = int(row[i], 16)
+            k += row[i + 1]
+    x2 = np.zeros((E, K, N), np.uint8)
+    for e in range(E):
+        for n in range(N):
+            x2[e, :, n] = int(g["x2_kn"][f"expert{e}"][f"col{n}"], 16)
+    sc = np.array(g["scale_pairs_per_col"], np.uint8)
+    if transpose:
+        x2, scale = x2.transpose(0, 2, 1).copy(), sc.reshape(N, 1, 2)
+    else:
+        scale = sc.reshape(1, N, 2)
+    shared = torch.tensor(g["shared_input_values"], dtype=torch.float32).to(torch.bfloat16)
+    spec = W.Spec("golden", batch=g["batch"], M=M, K=K, N=N, E=E, transpose_x2=transpose,
+                  shared_weight=g["shared_input_weight"])
+    inp = dict(x1=torch.from_numpy(x1), x2=torch.from_numpy(x2), scale=torch.from_numpy(scale),
+               pertoken_scale=torch.tensor(g["pertoken_scale_pairs"], dtype=torch.uint8).reshape(M, 1, 2),
+               group_list=torch.tensor(g["group_list_type1"]), logit=torch.tensor(g["logit"]),
+               row_index=torch.tensor(g["row_index"]), shared_input=shared,
+               out=torch.tensor(g["out_init"], dtype=torch.float32))
+    for det in (False, True):
+        got, bits = gpu_run(spec, inp, deterministic=det)
+        assert bits == 0
+        np.testing.assert_allclose(got, np.array(g["expected_out"]), rtol=0, atol=1e-5)
+
+
+# ----------------------------------------------------------------------------- small full-oracle cases
+SMALL = {
+    "basic": dict(),
+    "transposed": dict(transpose_x2=True),
+    "e5m2_prefix": dict(x1_dtype=W.E5M2, x2_dtype=W.E5M2, group_list_type=0, scale_lo=120, scale_hi=134),
+    "mixed_formats": dict(x1_dtype=W.E5M2, x2_dtype=W.E4M3, transpose_x2=True),
+    "per_expert_scale": dict(scale_per_expert=True),
+    "per_expert_scale_t": dict(scale_per_expert=True, transpose_x2=True, x1_dtype=W.E5M2, x2_dtype=W.E5M2),
+    "k96": dict(K=96),
+    "k160_t": dict(K=160, transpose_x2=True),
+    "k32_n8": dict(K=32, N=8),
+    "k16_n1": dict(K=16, N=1),
+    "ragged_counts": dict(E=8, M=63, counts="explicit", explicit_counts=(0, 1, 2, 4, 8, 16, 32, 0)),
+    "tokens_past_groups": dict(E=3, M=50, counts="explicit", explicit_counts=(10, 0, 20)),
+    "random_rows_shared": dict(rows="random", shared_rows=6, shared_offset=5, shared_weight=0.7, out_init="randn"),
+    "no_logit_no_shared": dict(logit="none", shared_rows=0),
+    "straddle": dict(E=9, M=1344, batch=200, N=256, K=128, rows="random",
+                     counts="explicit", explicit_counts=(63, 64, 65, 127, 128, 129, 255, 256, 257)),
+    "many_experts": dict(E=300, M=900, batch=300, N=128, K=128, counts="multinomial", rows="random"),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_atomic(name):
+    check_full(_spec(**SMALL[name]), W.make_inputs(_spec(**SMALL[name])))
+
+
+@pytest.mark.parametrize("name", ["basic", "transposed", "ragged_counts", "random_rows_shared", "straddle", "k96"])
+def test_small_deterministic(name):
+    spec = _spec(**SMALL[name])
+    inp = W.make_inputs(spec)
+    got, _ = check_full(spec, inp, deterministic=True)
+    again, _ = gpu_run(spec, inp, deterministic=True)
+    assert np.array_equal(got, again)
+
+
+@pytest.mark.parametrize("tmax", ["32", "64", "128"])
+def test_token_group_widths(tmax, monkeypatch):
+    monkeypatch.setenv("GMMFR_TMAX", tmax)
+    spec = _spec(**SMALL["straddle"])
+    check_full(spec, W.make_inputs(spec))
+
+
+def test_int32_row_index_and_raw_weights():
+    spec = _spec(rows="random", shared_rows=4, shared_offset=2)
+    inp = W.make_inputs(spec)
+    check_full(spec, inp, row_i32=True)
+    check_full(spec, inp, prepared=False)
+
+
+def test_m_zero_adds_only_shared():
+    spec = _spec(M=0, E=3, counts="explicit", explicit_counts=(0, 0, 0), out_init="randn")
+    check_full(spec, W.make_inputs(spec))
+
+
+def test_nan_scale_code_propagates():
+    spec = _spec(E=1, M=8, batch=8, logit="none", shared_rows=0)
+    inp = W.make_inputs(spec)
+    inp["pertoken_scale"][2, 1, 0] = 255
+    inp["scale"][0, 5, 1] = 255
+    got, ref = check_full(spec, inp)
+    assert np.isnan(got[2]).all() and np.isnan(got[:, 5]).all()
+
+
+def test_invalid_group_list_sets_error_and_clamps():
+    spec = _spec(E=4, M=40, counts="explicit", explicit_counts=(10, 10, 10, 10))
+    inp = W.make_inputs(spec)
+    inp["group_list"] = torch.tensor([12, -3, 25, 9], dtype=torch.int64)  # negative count, total > M
+    got, _ = check_full(spec, inp)
+    spec0 = dataclasses.replace(spec, group_list_type=0)
+    inp0 = dict(inp, group_list=torch.tensor([12, 8, 30, 45], dtype=torch.int64))  # decreasing, > M
+    check_full(spec0, inp0)
+
+
+def test_bad_row_index_sets_error_and_is_skipped():
+    spec = _spec(rows="random")
+    inp = W.make_inputs(spec)
+    inp["row_index"][3] = spec.batch
+    inp["row_index"][7] = -1
+    check_full(spec, inp)
+    check_full(spec, inp, deterministic=True)
+
+
+def test_prepared_layout_round_trip():
+    """The prepared tiles hold x2 and its scales at the documented positions
+    (bit-exact byte work), for both x2 layouts."""
+    for transpose in (False, True):
+        spec = _spec(K=200 - 200 % 16, N=200, E=2, transpose_x2=transpose)
+        inp = W.make_inputs(spec)
+        prob = B.problem_from_spec(spec)
+        d = _dev(inp)
+        buf = B.prepare_weights(prob, d["x2"], d["scale"]).cpu().numpy()
+        E, K, N = spec.E, spec.K, spec.N
+        NT, KB, Ks = -(-N // 128), -(-K // 128), spec.Ks
+        tiles = buf[:E * NT * KB * 16896].reshape(E, NT, KB, 16896)
+        x2 = inp["x2"].numpy()
+        x2_kn = x2.transpose(0, 2, 1) if transpose else x2  # -> [E, K, N]
+        sc = inp["scale"].numpy()
+        for e in range(E):
+            for j in range(NT):
+                for kb in range(KB):
+                    t = tiles[e, j, kb]
+                    r = np.arange(128)[:, None]
+                    c = np.arange(128)[None, :]
+                    w = t[(r * 128 + (((c // 16) ^ (r % 8)) * 16) + c % 16)]
+                    n, k = j * 128 + r, kb * 128 + c
+                    exp = np.where((n < N) & (k < K), x2_kn[e, np.minimum(k, K - 1), np.minimum(n, N - 1)], 0)
+                    assert np.array_equal(w, exp)
+                    q = np.arange(4)[None, :]
+                    s = t[16384 + 16 * (r % 32) + 4 * (r // 32) + q]
+                    g = kb * 4 + q
+                    nn = np.minimum(j * 128 + r, N - 1)
+                    kp, h = np.minimum(g // 2, Ks - 1), g % 2
+                    sv = sc[kp, nn, h] if not transpose else sc[nn, kp, h]
+                    exp_s = np.where(((j * 128 + r) < N) & (g * 32 < K), sv, 127)
+                    assert np.array_equal(s, exp_s)
+
+
+def test_timeout_path_reports_and_recovers(monkeypatch):
+    """A wait that nothing completes gives up after its limit, reports
+    GMMFR_DEV_TIMEOUT, and leaves the context usable."""
+    spec = _spec()
+    inp = W.make_inputs(spec)
+    monkeypatch.setenv("GMMFR_TEST_STALL_NS", "20000000")
+    _, bits = gpu_run(spec, inp)
+    assert bits & B.DEV_TIMEOUT
+    monkeypatch.delenv("GMMFR_TEST_STALL_NS")
+    check_full(spec, inp)
+
+
+# ----------------------------------------------------------------------------- benchmark workloads
+def test_config1_full():
+    spec = W.config(1)
+    check_full(spec, W.make_inputs(spec))
+
+
+@pytest.mark.parametrize("i", [2, 3, 4, 5])
+def test_config_sampled(i):
+    spec = W.config(i)
+    inp = W.make_inputs(spec, weights_device="cuda")
+    inp["x2"] = inp["x2"].cpu()
+    check_sampled(spec, inp)
+
+
+def test_config4_deterministic_bit_stable():
+    spec = W.config(4)
+    inp = W.make_inputs(spec, weights_device="cuda")
+    d = _dev(dict(inp, x2=inp["x2"]))
+    inp["x2"] = inp["x2"].cpu()
+    prob = B.problem_from_spec(spec, deterministic=True)
+    prep = B.prepare_weights(prob, d["x2"], d["scale"])
+    ws = B.workspace(prob, True, "cuda")
+    outs = []
+    for _ in range(5):
+        out = d["out"].clone()
+        B.run(prob, d, out, prepared=prep, ws=ws)
+        outs.append(out.cpu().numpy())
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    got = outs[0].astype(np.float64)
+    rng = np.random.default_rng(1)
+    rows, cols = rng.integers(0, spec.batch, 1024), rng.integers(0, spec.N, 1024)
+    ref, absb, _ = oracle.run_sampled(oracle.problem_from_spec(spec, inp), rows, cols)
+    init, sh = _extra_terms(spec, inp)
+    assert_close(got[rows, cols], ref, oracle.tolerance(ref, absb, init[rows, cols], sh[rows, cols]))
