@@ -29,6 +29,24 @@ METRIC = "µs/call and achieved HBM GB/s vs roofline, MXFP8 grouped-matmul-final
 DEFAULT_CONFIG = 2
 
 
+def reduce_step_time(ms: float, world: int) -> float:
+    """Slowest rank's mean step time (the job's step time).  Replicas share no
+    data: the only cross-rank operation is this max."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank: int, ms: float, world: int) -> float:
+    """Whole-job GB/s: every rank processes one call's bytes per step."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -229,11 +247,7 @@ def run_ours(args):
         dist.barrier()
     kernel_ms = B.gmmfr_profile_end(args.steps)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_step_time(statistics.mean(step_ms), world)
     gemm_ms = statistics.mean(k[2] for k in kernel_ms)
     pro_ms = statistics.mean(k[1] for k in kernel_ms)
     comb = [k[3] for k in kernel_ms if k[3] >= 0]
@@ -266,7 +280,7 @@ def run_ours(args):
 
     peaks, peak_kind = _peaks()
     hbm_peak = float(peaks["hbm_gbs"])
-    gbs = alg_bytes / (ms * 1e-3) / 1e9 * world
+    gbs = job_throughput(alg_bytes, ms, world)
     gemm_gbs = alg_bytes / (gemm_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
