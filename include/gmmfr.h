@@ -162,6 +162,36 @@ GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing(
  */
 GMMFR_API gmmfr_status gmmfr_check_device_errors(const void* workspace, void* stream, uint32_t* bits);
 
+/*
+ * Allocation-free form of gmmfr_grouped_matmul_finalize_routing (no counterpart on
+ * the source pages; added for callers that must not allocate device memory).
+ *
+ * Some callers cannot hand us a workspace: code embedded in a host runtime whose
+ * memory pool owns the whole device and forbids outside allocations, serving
+ * loops where a cudaMalloc (which can synchronise the device and fail under
+ * memory pressure) is not acceptable, or plain C callers without an allocator.
+ * This call takes the same tensors as the operator minus x2, scale and the
+ * workspace, and uses instead a 16 MiB scratch array compiled into the library
+ * as a file-scope __device__ variable.  Every GPU that loads the library holds
+ * those 16 MiB until the process exits.  It calls no cudaMalloc / cudaFree.
+ *
+ *   prepared   required: weights from gmmfr_prepare_weights (the call cannot prepare
+ *              them itself); other arguments as for the operator.
+ * Problems whose workspace (gmmfr_workspace_size with have_prepared = 1) exceeds
+ * 16 MiB are rejected with GMMFR_ERR_WORKSPACE and a message giving both sizes.
+ * The first call on each device resolves the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls share the one array and it keeps the last call's
+ * contents (the operator rewrites every word it reads, so nothing needs
+ * clearing); calls that can overlap on the GPU (different streams, or several
+ * host threads) race on it and must be serialised by the caller.  The device
+ * error word of these calls lives in that array and is not exposed.
+ */
+GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing_static_scratch(
+    const gmmfr_problem* problem, const void* x1, const void* pertoken_scale, const int64_t* group_list,
+    const float* logit, const void* row_index, const void* shared_input, float* out, const void* prepared,
+    void* stream);
+
 /* Message of the last error returned on the calling thread ("" if none). */
 GMMFR_API const char* gmmfr_last_error(void);
 

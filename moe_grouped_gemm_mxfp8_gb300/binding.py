@@ -28,7 +28,7 @@ PROFILE_SLOT_NAMES = ("prep", "prologue", "gemm", "combine")
 ENTRY_POINTS = (
     "gmmfr_prepared_weights_size", "gmmfr_prepare_weights", "gmmfr_workspace_size",
     "gmmfr_grouped_matmul_finalize_routing", "gmmfr_check_device_errors", "gmmfr_last_error",
-    "gmmfr_profile_begin", "gmmfr_profile_end",
+    "gmmfr_profile_begin", "gmmfr_profile_end", "gmmfr_grouped_matmul_finalize_routing_static_scratch",
 )
 
 
@@ -69,6 +69,7 @@ def load(path: str = LIB_PATH):
             lib.gmmfr_prepare_weights.argtypes = [P, vp, vp, vp, sz, vp]
             lib.gmmfr_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
             lib.gmmfr_grouped_matmul_finalize_routing.argtypes = [P] + [vp] * 11 + [sz, vp]
+            lib.gmmfr_grouped_matmul_finalize_routing_static_scratch.argtypes = [P] + [vp] * 9
             lib.gmmfr_check_device_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
             lib.gmmfr_last_error.restype = ctypes.c_char_p
             lib.gmmfr_profile_begin.argtypes = [ctypes.c_int]
@@ -133,6 +134,16 @@ def gmmfr_grouped_matmul_finalize_routing(problem: Problem, x1, x2, scale, perto
     _check(load().gmmfr_grouped_matmul_finalize_routing(
         ctypes.byref(problem), x1, x2, scale, pertoken_scale, group_list, logit, row_index, shared_input,
         out, prepared, workspace, workspace_bytes, stream))
+
+
+def gmmfr_grouped_matmul_finalize_routing_static_scratch(problem: Problem, x1, pertoken_scale, group_list, logit,
+                                                         row_index, shared_input, out, prepared,
+                                                         stream=None) -> None:
+    """The operator with the library's own 16 MiB device scratch instead of a
+    caller workspace (for callers that cannot allocate); needs prepared weights."""
+    _check(load().gmmfr_grouped_matmul_finalize_routing_static_scratch(
+        ctypes.byref(problem), x1, pertoken_scale, group_list, logit, row_index, shared_input, out, prepared,
+        stream))
 
 
 def gmmfr_check_device_errors(workspace: int, stream: Optional[int] = None) -> int:

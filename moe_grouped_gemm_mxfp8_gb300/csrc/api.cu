@@ -166,6 +166,11 @@ bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 
 }  // namespace
 
+namespace gmmfr {
+// Records `message` as the calling thread's last error (for other files of the library).
+gmmfr_status record_error(gmmfr_status st, const char* message) { return fail(st, "%s", message); }
+}  // namespace gmmfr
+
 extern "C" {
 
 const char* gmmfr_last_error(void) { return g_last_error.c_str(); }

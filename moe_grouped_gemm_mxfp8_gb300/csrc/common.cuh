@@ -96,5 +96,10 @@ cudaError_t launch_prologue(const PrologueParams& p, int grid, cudaStream_t s);
 cudaError_t launch_gemm(const CUtensorMap& tmap_x1, const GemmParams& p, int tmax, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 int gemm_smem_bytes(int tmax);
+}  // namespace gmmfr
+
+#include "gmmfr.h"
+namespace gmmfr {
+gmmfr_status record_error(gmmfr_status st, const char* message);
 
 }  // namespace gmmfr

@@ -1,0 +1,66 @@
+// Allocation-free form of the operator, for callers that must not allocate
+// device memory themselves: the scratch space the kernels need lives in one
+// file-scope device array that every GPU loading the library holds until the
+// process exits.
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "gmmfr.h"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr int kMaxDevices = 64;
+
+// Device scratch shared by every call of the allocation-free entry point.
+// In host code this name is only a stand-in for the symbol: its device address
+// comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing_static_scratch(
+    const gmmfr_problem* problem, const void* x1, const void* pertoken_scale, const int64_t* group_list,
+    const float* logit, const void* row_index, const void* shared_input, float* out, const void* prepared,
+    void* stream) {
+  size_t need = 0;
+  if (gmmfr_status st = gmmfr_workspace_size(problem, 1, &need)) return st;
+  if (!prepared)
+    return gmmfr::record_error(GMMFR_ERR_INVALID_ARG,
+                               "the static-scratch entry point needs weights from gmmfr_prepare_weights");
+  if (need > kStaticScratchBytes) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "problem needs %zu bytes of scratch; the static scratch holds %zu (16 MiB)", need,
+             kStaticScratchBytes);
+    return gmmfr::record_error(GMMFR_ERR_WORKSPACE, msg);
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return gmmfr::record_error(GMMFR_ERR_CUDA, cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return gmmfr::record_error(GMMFR_ERR_UNSUPPORTED, "device index above 63");
+  void* scratch = nullptr;
+  {
+    // once per device, with that device current: resolve the array's device address
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_scratch_ptr[dev]) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+      if (e != cudaSuccess || !ptr) {
+        char msg[256];
+        snprintf(msg, sizeof(msg), "cudaGetSymbolAddress of the static scratch failed: %s", cudaGetErrorString(e));
+        return gmmfr::record_error(GMMFR_ERR_CUDA, msg);
+      }
+      g_scratch_ptr[dev] = ptr;
+    }
+    scratch = g_scratch_ptr[dev];
+  }
+  // The operator overwrites every scratch word it reads (header, group table,
+  // token scales, CSR) before reading it, so nothing has to be cleared here.
+  return gmmfr_grouped_matmul_finalize_routing(problem, x1, nullptr, nullptr, pertoken_scale, group_list, logit,
+                                               row_index, shared_input, out, prepared, scratch,
+                                               kStaticScratchBytes, stream);
+}
