@@ -112,17 +112,8 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def _cpu_baseline(spec, inp, target_s=10.0):
-    """The oracle, as it stands, on a column slice of the workload (all host
-    cores); returns (GB/s scaled to the whole workload, seconds, sample text, cores)."""
-    import numpy as np
-    import torch
-
+def _oracle_problem(spec, inp, ncols):
     import oracle
-    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
-
-    threads = oracle.num_threads()
-    ncols = min(spec.N, 64 * max(1, threads))
     x2 = inp["x2"].cpu()
     sc = inp["scale"].cpu()
     if spec.transpose_x2:
@@ -132,19 +123,64 @@ def _cpu_baseline(spec, inp, target_s=10.0):
         x2s = x2[:, :, :ncols].contiguous()
         scs = sc[..., :ncols, :].contiguous()
     shared = inp["shared_input"][:, :ncols].contiguous() if inp["shared_input"] is not None else None
-    p = oracle.Problem(M=spec.M, K=spec.K, N=ncols, E=spec.E, batch=spec.batch, x1=inp["x1"].cpu(), x2=x2s,
-                       scale=scs, pertoken_scale=inp["pertoken_scale"].cpu(), group_list=inp["group_list"].cpu(),
-                       row_index=inp["row_index"].cpu(), out=inp["out"].cpu()[:, :ncols].contiguous(),
-                       x1_dtype=spec.x1_dtype, x2_dtype=spec.x2_dtype, transpose_x2=spec.transpose_x2,
-                       scale_per_expert=spec.scale_per_expert, group_list_type=spec.group_list_type,
-                       logit=inp["logit"].cpu() if inp["logit"] is not None else None, shared_input=shared,
-                       shared_offset=spec.shared_offset, shared_weight=spec.shared_weight)
+    return oracle.Problem(M=spec.M, K=spec.K, N=ncols, E=spec.E, batch=spec.batch, x1=inp["x1"].cpu(), x2=x2s,
+                          scale=scs, pertoken_scale=inp["pertoken_scale"].cpu(), group_list=inp["group_list"].cpu(),
+                          row_index=inp["row_index"].cpu(), out=inp["out"].cpu()[:, :ncols].contiguous(),
+                          x1_dtype=spec.x1_dtype, x2_dtype=spec.x2_dtype, transpose_x2=spec.transpose_x2,
+                          scale_per_expert=spec.scale_per_expert, group_list_type=spec.group_list_type,
+                          logit=inp["logit"].cpu() if inp["logit"] is not None else None, shared_input=shared,
+                          shared_offset=spec.shared_offset, shared_weight=spec.shared_weight)
+
+
+def _cpu_baseline(spec, inp, min_s=10.0, max_s=30.0):
+    """The oracle, as it stands, on all host cores: the whole workload (repeated
+    until about min_s of work) when a probe predicts it takes at most max_s,
+    otherwise a slice of output columns sized for about min_s, scaled by N/cols.
+    Returns (GB/s for the whole workload, seconds, sample text, cores)."""
+    import oracle
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+    threads = oracle.num_threads()
+    probe_cols = min(spec.N, 64 * max(1, threads))
     t0 = time.perf_counter()
-    oracle.run(p)
+    oracle.run(_oracle_problem(spec, inp, probe_cols))
+    probe = time.perf_counter() - t0
+    est_full = probe * spec.N / probe_cols
+    if est_full <= max_s:
+        ncols, reps = spec.N, max(1, int(min_s / max(est_full, 1e-3)))
+    else:
+        ncols, reps = min(spec.N, max(probe_cols, int(probe_cols * min_s / max(probe, 1e-3)) // 64 * 64)), 1
+    p = _oracle_problem(spec, inp, ncols)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.run(p)
     dt = time.perf_counter() - t0
-    full_s = dt * spec.N / ncols
-    gbs = W.algorithmic_bytes(spec) / full_s / 1e9
-    return gbs, dt, f"oracle on output columns [0,{ncols}) of {spec.N} ({dt:.1f} s), scaled by N/{ncols}", threads
+    per_call = dt / reps * spec.N / ncols
+    gbs = W.algorithmic_bytes(spec) / per_call / 1e9
+    what = "the whole workload" if ncols == spec.N else f"output columns [0,{ncols}) of {spec.N}, scaled by N/{ncols}"
+    return gbs, dt, f"oracle on {what}, {reps} run(s), {dt:.1f} s", threads
+
+
+def _profiled_traffic(workload):
+    """DRAM bytes per gemm_kernel launch from the committed ncu summary of this
+    workload, if the kernel sources are unchanged since that capture (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_kernel_" + workload.split()[0] + ".md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    h = hashlib.sha256()
+    for f in ("kernels_gemm.cu", "ptx.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "moe_grouped_gemm_mxfp8_gb300", "csrc", f), "rb").read())
+    want = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("source-sha256-16", "traffic-bytes-per-launch")):
+            k, v = line.strip().strip("`").split(":", 1)
+            want[k.strip()] = v.strip().strip("`")
+    if want.get("source-sha256-16") != h.hexdigest()[:16]:
+        return None
+    return int(want["traffic-bytes-per-launch"]) if "traffic-bytes-per-launch" in want else None
 
 
 def run_reference(args):
@@ -227,6 +263,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     bits = B.gmmfr_check_device_errors(ws.data_ptr(), sptr)
 
+    sleep_cycles = 200000  # about 0.1 ms at 2 GHz
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     B.gmmfr_profile_begin(args.steps)
@@ -238,6 +275,9 @@ def run_ours(args):
         for i in range(args.steps):
             flush.zero_()
             out.copy_(out0)
+            # keep the GPU busy while the host enqueues the call, so the events
+            # time the device work of the call, not the host's launch latency
+            torch.cuda._sleep(sleep_cycles)
             starts[i].record()
             call(out)
             ends[i].record()
@@ -247,9 +287,12 @@ def run_ours(args):
         dist.barrier()
     kernel_ms = B.gmmfr_profile_end(args.steps)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = reduce_step_time(statistics.mean(step_ms), world)
+    # device time of a call: start of its first kernel to end of its last (library events)
+    call_ms = [k[4] for k in kernel_ms]
+    ms = reduce_step_time(statistics.mean(call_ms), world)
     gemm_ms = statistics.mean(k[2] for k in kernel_ms)
-    pro_ms = statistics.mean(k[1] for k in kernel_ms)
+    route = [k[1] for k in kernel_ms if k[1] >= 0]
+    pro_ms = statistics.mean(route) if route else None
     comb = [k[3] for k in kernel_ms if k[3] >= 0]
     comb_ms = statistics.mean(comb) if comb else None
 
@@ -287,18 +330,19 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8 (fp8 x fp8, e8m0 per 32) -> f32", "data": "synthetic",
         "config": _config_dict(spec, counts, args.deterministic),
-        "us_per_call": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12,
+        "us_per_call": ms * 1e3, "us_per_call_min": min(call_ms) * 1e3,
+        "us_per_step_events": statistics.mean(step_ms) * 1e3, "tflops": flops / (ms * 1e-3) / 1e12,
         "roofline_fraction_call": gbs / world / hbm_peak,
-        "kernels_ms": {"prologue": pro_ms, "gemm": gemm_ms, "combine": comb_ms},
+        "kernels_ms": {"route": pro_ms, "gemm": gemm_ms, "combine": comb_ms},
         "weight_prep_ms": prep_ms,
         "weight_prep_gbs": 2 * n_prep / (prep_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": gemm_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": gemm_gbs / hbm_peak, "traffic": None,
+                     "frac": gemm_gbs / hbm_peak, "traffic": _profiled_traffic(spec.name),
                      "kernel": "gemm_kernel (grouped GEMM + fused epilogue)",
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
         "e2e": {"value": alg_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * (3 if args.deterministic else 2),
+        "gpu_launches": args.steps * (3 if args.deterministic else 1),
         "device_error_bits": bits,
         "clocks": clk.summary(),
         "wall_s_timed": t_wall,

@@ -201,10 +201,11 @@ GMMFR_API const char* gmmfr_last_error(void);
  * kernels on its stream.  gmmfr_profile_end SYNCHRONISES the device, writes
  * ms[call * GMMFR_PROFILE_SLOTS + slot] (-1 where a slot's kernel did not run),
  * sets *n_calls, and stops recording.
- * Slots: 0 weight preparation inside the call, 1 prologue (group ranges and
- * token-scale layout), 2 grouped GEMM with fused epilogue, 3 deterministic combine.
+ * Slots: 0 weight preparation inside the call, 1 deterministic-mode routing (row
+ * CSR of the tokens), 2 grouped GEMM with fused epilogue, 3 deterministic combine,
+ * 4 the whole call (start of its first kernel to end of its last).
  */
-#define GMMFR_PROFILE_SLOTS 4
+#define GMMFR_PROFILE_SLOTS 5
 GMMFR_API gmmfr_status gmmfr_profile_begin(int max_calls);
 GMMFR_API gmmfr_status gmmfr_profile_end(float* ms, int max_entries, int* n_calls);
 

@@ -21,8 +21,8 @@ E4M3, E5M2 = 0, 1
 INDEX_I64, INDEX_I32 = 0, 1
 DETERMINISTIC = 1
 DEV_BAD_GROUP_LIST, DEV_BAD_ROW_INDEX, DEV_TIMEOUT = 1, 2, 4
-PROFILE_SLOTS = 4
-PROFILE_SLOT_NAMES = ("prep", "prologue", "gemm", "combine")
+PROFILE_SLOTS = 5
+PROFILE_SLOT_NAMES = ("prep", "route", "gemm", "combine", "call")
 
 # exported entry points, as declared in include/gmmfr.h
 ENTRY_POINTS = (

@@ -1,6 +1,6 @@
 // C ABI of the MXFP8 grouped-matmul-finalize-routing library (declared in
 // include/gmmfr.h): argument checks, workspace layout, tensor map of x1, and the
-// launch sequence prologue -> grouped GEMM -> (deterministic) combine.
+// launch sequence (deterministic routing ->) grouped GEMM (-> deterministic combine).
 #include "gmmfr.h"
 
 #include <cudaTypedefs.h>
@@ -68,20 +68,20 @@ int device_sms() {
   return sms;
 }
 
-int choose_tmax(const gmmfr_problem* p) {
+// Token group width fixed by the caller for tests (GMMFR_TMAX = 32, 64 or 128); 0 lets the
+// kernel pick the smallest width that holds the largest expert.
+int fixed_tmax() {
   if (const char* s = std::getenv("GMMFR_TMAX")) {
     const int v = std::atoi(s);
     if (v == 32 || v == 64 || v == 128) return v;
   }
-  const int64_t avg = cdiv(p->M, p->E);
-  return avg <= 32 ? 64 : 128;
+  return 0;
 }
 
 struct Layout {
   int64_t NT, KB, Ks;
-  int tmax, split;
-  int64_t max_groups;
-  size_t off_groups, off_tsf, off_cnt, off_rowptr, off_cursor, off_sorted, off_y, off_prep, total;
+  int split;
+  size_t off_cnt, off_rowptr, off_cursor, off_sorted, off_y, off_prep, total;
 };
 
 Layout make_layout(const gmmfr_problem* p, bool have_prepared) {
@@ -89,8 +89,6 @@ Layout make_layout(const gmmfr_problem* p, bool have_prepared) {
   L.NT = cdiv(p->N, gmmfr::kTileN);
   L.KB = cdiv(p->K, gmmfr::kTileK);
   L.Ks = cdiv(p->K, 64);
-  L.tmax = choose_tmax(p);
-  L.max_groups = p->E + cdiv(p->M, L.tmax);
   const bool det = p->flags & GMMFR_DETERMINISTIC;
   if (det) {
     const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(p->E, std::max<int64_t>(p->M, 1)) * L.NT);
@@ -99,10 +97,6 @@ Layout make_layout(const gmmfr_problem* p, bool have_prepared) {
     L.split = 1;
   }
   size_t off = gmmfr::kHdrBytes;
-  L.off_groups = off;
-  off = align256(off + sizeof(int4) * (size_t)L.max_groups);
-  L.off_tsf = off;
-  off = align256(off + (size_t)L.max_groups * L.KB * gmmfr::kSfChunk);
   if (det) {
     L.off_cnt = off;
     off = align256(off + sizeof(int32_t) * (size_t)p->batch);
@@ -256,6 +250,7 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   cudaError_t e;
 
   const uint8_t* wprep = static_cast<const uint8_t*>(prepared);
+  timer.begin(4, s);
   if (!prepared) {
     timer.begin(0, s);
     e = gmmfr::launch_prep(prep_params(problem, x2, scale, ws + L.off_prep), s);
@@ -264,61 +259,53 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
     wprep = ws + L.off_prep;
   }
 
-  // x1 [M, K] bytes as a 2-D tensor, 16-row x 128-byte boxes, 128-byte swizzle
-  CUtensorMap tmap;
+  // x1 [M, K] bytes as 2-D tensors of 128-byte rows: boxes of 16, 32, 64, 128 rows, 128-byte swizzle
+  gmmfr::TokenMaps tmaps;
   {
     const bool empty = p.M == 0;
     cuuint64_t dims[2] = {(cuuint64_t)(empty ? 16 : p.K), (cuuint64_t)(empty ? 1 : p.M)};
     cuuint64_t strides[1] = {(cuuint64_t)(empty ? 16 : p.K)};
-    cuuint32_t box[2] = {(cuuint32_t)gmmfr::kTileK, (cuuint32_t)gmmfr::kTokBox};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, empty ? (void*)ws : const_cast<void*>(x1), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(GMMFR_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    for (int b = 0; b < 4; ++b) {
+      cuuint32_t box[2] = {(cuuint32_t)gmmfr::kTileK, (cuuint32_t)(gmmfr::kTokBox << b)};
+      CUresult r = encode(&tmaps.m[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, empty ? (void*)ws : const_cast<void*>(x1), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(GMMFR_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
   }
 
-  gmmfr::PrologueParams pp{};
-  pp.group_list = group_list;
-  pp.pertoken_scale = static_cast<const uint8_t*>(pertoken_scale);
-  pp.row_index = row_index;
-  pp.hdr = hdr;
-  pp.groups = reinterpret_cast<int4*>(ws + L.off_groups);
-  pp.tsf = ws + L.off_tsf;
+  int32_t* row_ptr = det ? reinterpret_cast<int32_t*>(ws + L.off_rowptr) : nullptr;
+  int32_t* sorted = det ? reinterpret_cast<int32_t*>(ws + L.off_sorted) : nullptr;
   if (det) {
-    pp.cnt = reinterpret_cast<int32_t*>(ws + L.off_cnt);
-    pp.row_ptr = reinterpret_cast<int32_t*>(ws + L.off_rowptr);
-    pp.cursor = reinterpret_cast<int32_t*>(ws + L.off_cursor);
-    pp.sorted = reinterpret_cast<int32_t*>(ws + L.off_sorted);
+    gmmfr::RouteParams rp{};
+    rp.group_list = group_list;
+    rp.row_index = row_index;
+    rp.cnt = reinterpret_cast<int32_t*>(ws + L.off_cnt);
+    rp.row_ptr = row_ptr;
+    rp.cursor = reinterpret_cast<int32_t*>(ws + L.off_cursor);
+    rp.sorted = sorted;
+    rp.M = p.M;
+    rp.batch = p.batch;
+    rp.E = (int32_t)p.E;
+    rp.group_list_type = p.group_list_type;
+    rp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;
+    timer.begin(1, s);
+    e = gmmfr::launch_route(rp, s);
+    timer.end(1, s);
+    if (e != cudaSuccess) return cuda_fail(e, "routing launch");
   }
-  pp.M = p.M;
-  pp.K = p.K;
-  pp.batch = p.batch;
-  pp.E = (int32_t)p.E;
-  pp.KB = (int32_t)L.KB;
-  pp.Ks = (int32_t)L.Ks;
-  pp.tmax = L.tmax;
-  pp.group_list_type = p.group_list_type;
-  pp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;
-  pp.deterministic = det;
-  const int64_t sf_items = L.max_groups * L.KB;
-  const int pro_grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, cdiv(sf_items, 8)));
-  timer.begin(1, s);
-  e = gmmfr::launch_prologue(pp, pro_grid, s);
-  timer.end(1, s);
-  if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
 
   gmmfr::GemmParams gp{};
   gp.prepared = wprep;
-  gp.tsf = ws + L.off_tsf;
-  gp.groups = reinterpret_cast<const int4*>(ws + L.off_groups);
+  gp.group_list = group_list;
+  gp.pertoken_scale = static_cast<const uint8_t*>(pertoken_scale);
   gp.hdr = hdr;
   gp.logit = logit;
   gp.row_index = row_index;
   gp.shared = static_cast<const uint16_t*>(shared_input);
   gp.out = out;
   gp.ybuf = det ? reinterpret_cast<float*>(ws + L.off_y) : nullptr;
-  gp.err = hdr + gmmfr::kHdrErr;
   gp.M = p.M;
   gp.N = p.N;
   gp.K = p.K;
@@ -326,8 +313,12 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   gp.shared_rows = shared_input ? p.shared_rows : 0;
   gp.shared_offset = p.shared_offset;
   gp.shared_weight = p.shared_weight;
+  gp.E = (int32_t)p.E;
+  gp.group_list_type = p.group_list_type;
   gp.NT = (int32_t)L.NT;
   gp.KB = (int32_t)L.KB;
+  gp.Ks = (int32_t)L.Ks;
+  gp.tmax_fixed = fixed_tmax();
   gp.split = L.split;
   gp.deterministic = det;
   gp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;
@@ -341,15 +332,14 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
     gp.timeout_ns = std::atoll(t) > 0 ? std::atoll(t) : 1000000;
   }
   timer.begin(2, s);
-  e = gmmfr::launch_gemm(tmap, gp, L.tmax, sms, s);
+  e = gmmfr::launch_gemm(tmaps, gp, std::min(sms, gmmfr::kMaxErrSlots), s);
   timer.end(2, s);
   if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
 
   if (det) {
     gmmfr::CombineParams cp{};
-    cp.hdr = hdr;
-    cp.row_ptr = pp.row_ptr;
-    cp.sorted = pp.sorted;
+    cp.row_ptr = row_ptr;
+    cp.sorted = sorted;
     cp.ybuf = gp.ybuf;
     cp.shared = gp.shared;
     cp.out = out;
@@ -365,16 +355,20 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
     timer.end(3, s);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
+  timer.end(4, s);
   return GMMFR_OK;
 }
 
 gmmfr_status gmmfr_check_device_errors(const void* workspace, void* stream, uint32_t* bits) {
   if (!workspace || !bits) return fail(GMMFR_ERR_INVALID_ARG, "workspace and bits must be non-NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t v = 0;
-  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+  std::vector<uint32_t> h(gmmfr::kHdrBytes / 4);
+  cudaError_t e = cudaMemcpyAsync(h.data(), workspace, gmmfr::kHdrBytes, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error words");
+  const uint32_t n = std::min<uint32_t>(h[0], gmmfr::kMaxErrSlots);
+  uint32_t v = 0;
+  for (uint32_t i = 0; i < n; ++i) v |= h[1 + i];
   *bits = v;
   if (v) return fail(GMMFR_ERR_DEVICE, "device error bits 0x%x", v);
   return GMMFR_OK;

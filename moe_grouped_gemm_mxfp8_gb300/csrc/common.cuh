@@ -14,13 +14,13 @@ constexpr int kWTileBytes = kTileN * kTileK;  // 16 KB of FP8 weights per tile
 constexpr int kSfChunk = 512;              // scale bytes of a 128-row x 4-block tile
 constexpr int kPrepTileBytes = kWTileBytes + kSfChunk;  // 16896: prepared tile = weights + scales
 constexpr int kTokBox = 16;                // token rows per TMA box
-constexpr int kGemmThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kGemmThreads = 224;          // warp 0 TMA, 1 MMA, 2..5 epilogue, 6 token-scale packer
+constexpr int kMaxExperts = 1024;
 
-// header words at the start of the workspace
-constexpr int kHdrErr = 0;      // uint32 device error bits
-constexpr int kHdrGroups = 1;   // number of token groups
-constexpr int kHdrCovered = 2;  // tokens covered by the expert ranges
-constexpr int kHdrBytes = 256;
+// Workspace header: word 0 = number of error slots written by the last GEMM
+// launch, words 1..kMaxErrSlots = each CTA's device error bits.
+constexpr int kMaxErrSlots = 1023;
+constexpr int kHdrBytes = 4096;
 
 constexpr uint32_t kErrBadGroupList = 1u;
 constexpr uint32_t kErrBadRowIndex = 2u;
@@ -36,49 +36,45 @@ struct PrepParams {
   int32_t scale_per_expert;
 };
 
-struct PrologueParams {
+// Deterministic mode: tokens of each out row (CSR, unordered within a row).
+struct RouteParams {
   const int64_t* group_list;
-  const uint8_t* pertoken_scale;  // [M, 2*Ks]
   const void* row_index;
-  uint32_t* hdr;
-  int4* groups;                   // {expert, first token, tokens, 0}
-  uint8_t* tsf;                   // [groups][KB][512]
-  int32_t* cnt;                   // deterministic CSR scratch
+  int32_t* cnt;
   int32_t* row_ptr;
   int32_t* cursor;
   int32_t* sorted;
-  int64_t M, K, batch;
-  int32_t E, KB, Ks, tmax;
+  int64_t M, batch;
+  int32_t E;
   int32_t group_list_type;
   int32_t row_i32;
-  int32_t deterministic;
 };
 
 struct GemmParams {
   const uint8_t* prepared;
-  const uint8_t* tsf;
-  const int4* groups;
-  const uint32_t* hdr;
+  const int64_t* group_list;
+  const uint8_t* pertoken_scale;  // [M, 2*Ks]
   const float* logit;
   const void* row_index;
   const uint16_t* shared;  // bf16 bits; added here only in atomic mode
   float* out;
   float* ybuf;             // deterministic: [split][M][N]
-  uint32_t* err;
+  uint32_t* hdr;           // error slots (see kHdrBytes)
   int64_t M, N, K, batch;
   int64_t shared_rows, shared_offset;
   float shared_weight;
-  int32_t NT, KB;
+  int32_t E, group_list_type;
+  int32_t NT, KB, Ks;
   int32_t split;           // deterministic K split count
   int32_t deterministic;
   int32_t row_i32;
+  int32_t tmax_fixed;      // 0: token group width chosen on the device from the largest expert
   uint32_t idesc;          // instruction descriptor without N and scale-factor ids
   int64_t timeout_ns;
   int32_t test_stall;      // testing aid: wait on a barrier nothing arrives on
 };
 
 struct CombineParams {
-  const uint32_t* hdr;
   const int32_t* row_ptr;
   const int32_t* sorted;
   const float* ybuf;
@@ -92,10 +88,14 @@ struct CombineParams {
 
 // launchers (defined next to their kernels)
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
-cudaError_t launch_prologue(const PrologueParams& p, int grid, cudaStream_t s);
-cudaError_t launch_gemm(const CUtensorMap& tmap_x1, const GemmParams& p, int tmax, int grid, cudaStream_t s);
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
+// x1 [M, K] as 2-D tensors of 128-byte rows, boxes of 16, 32, 64 and 128 rows (128-byte swizzle).
+struct TokenMaps {
+  CUtensorMap m[4];
+};
+cudaError_t launch_gemm(const TokenMaps& tmaps, const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
-int gemm_smem_bytes(int tmax);
+int gemm_smem_bytes();
 }  // namespace gmmfr
 
 #include "gmmfr.h"

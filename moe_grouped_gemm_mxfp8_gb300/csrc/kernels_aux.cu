@@ -1,7 +1,6 @@
 // Auxiliary kernels of MXFP8 grouped-matmul-finalize-routing:
 //   - weight preparation (one-time re-layout of x2 and its scales into GEMM tiles),
-//   - per-call prologue (group_list decode and checks, token groups, token-scale
-//     layout for the tensor cores, and the row CSR of the deterministic mode),
+//   - deterministic-mode routing (row CSR of the routed tokens),
 //   - deterministic combine (row-ordered sum of the per-token results).
 #include "common.cuh"
 
@@ -107,131 +106,57 @@ __device__ __forceinline__ int64_t load_row(const void* rows, int row_i32, int64
   return row_i32 ? (int64_t) static_cast<const int32_t*>(rows)[t] : static_cast<const int64_t*>(rows)[t];
 }
 
-// Every block decodes the (at most 1024) expert ranges itself; block 0 also
-// publishes the group table and header; all blocks then lay out token scales;
-// in deterministic mode the last block builds the row CSR.
-__global__ void __launch_bounds__(1024) prologue_kernel(PrologueParams p) {
+// Deterministic mode: one block of 1024 threads decodes the expert ranges (as
+// the GEMM kernel does: contiguous, clamped to [0, M]) to find the covered
+// tokens [0, covered), then builds the CSR of covered tokens by out row.
+// Positions within a row come from atomics; the combine kernel orders them.
+__global__ void __launch_bounds__(1024) route_kernel(RouteParams p) {
   __shared__ int64_t s_warp[32];
-  __shared__ int64_t s_start[1024];
-  __shared__ int64_t s_end[1024];
-  __shared__ int32_t s_gbase[1025];
-  __shared__ uint32_t s_err;
+  __shared__ int64_t s_covered;
   const int tid = threadIdx.x;
-  const int E = p.E;
   const int64_t M = p.M;
-  if (tid == 0) s_err = 0;
-  __syncthreads();
-
-  // ---- expert ranges (contiguous, clamped to [0, M]; section 4.3 group_list formats)
-  const int64_t g = tid < E ? p.group_list[tid] : 0;
+  const int64_t g = tid < p.E ? p.group_list[tid] : 0;
   int64_t end;
   if (p.group_list_type == 1) {
-    // counts: end_e = min(sum_{i<=e} max(g_i,0), M); saturate each term at M+1
-    const int64_t c = tid < E ? (g < 0 ? 0 : (g > M ? M + 1 : g)) : 0;
-    if (tid < E && g < 0) atomicOr(&s_err, kErrBadGroupList);
+    const int64_t c = tid < p.E ? (g < 0 ? 0 : (g > M ? M + 1 : g)) : 0;
     const int64_t incl = block_scan_incl<false>(c, s_warp);
-    if (tid == E - 1 && incl > M) atomicOr(&s_err, kErrBadGroupList);
     end = incl < M ? incl : M;
   } else {
-    // prefix sums: end_e = min(max(0, g_0..g_e), M)
-    const int64_t prev = (tid > 0 && tid < E) ? p.group_list[tid - 1] : 0;
-    if (tid < E && (g < prev || g > M)) atomicOr(&s_err, kErrBadGroupList);
-    const int64_t c = tid < E ? (g < 0 ? 0 : (g > M ? M : g)) : 0;
+    const int64_t c = tid < p.E ? (g < 0 ? 0 : (g > M ? M : g)) : 0;
     const int64_t incl = block_scan_incl<true>(c, s_warp);
     end = incl < M ? incl : M;
   }
-  s_end[tid] = end;
+  if (tid == p.E - 1) s_covered = end;
+  for (int64_t r = tid; r < p.batch; r += blockDim.x) p.cnt[r] = 0;
   __syncthreads();
-  const int64_t start = tid == 0 ? 0 : s_end[tid - 1];
-  s_start[tid] = start;
-  const int64_t cnt = tid < E ? end - start : 0;
-  const int64_t ng = (cnt + p.tmax - 1) / p.tmax;
-  const int64_t gincl = block_scan_incl<false>(ng, s_warp);
-  s_gbase[tid + 1] = (int32_t)gincl;
-  if (tid == 0) s_gbase[0] = 0;
+  const int64_t covered = s_covered;
+  for (int64_t t = tid; t < covered; t += blockDim.x) {
+    const int64_t r = load_row(p.row_index, p.row_i32, t);
+    if (r >= 0 && r < p.batch) atomicAdd(&p.cnt[r], 1);
+  }
   __syncthreads();
-  const int n_groups = s_gbase[E];
-  const int64_t covered = s_end[E - 1];
-
-  if (blockIdx.x == 0) {
-    if (tid < E) {
-      const int gb = s_gbase[tid];
-      for (int i = 0; i < ng; ++i) {
-        const int64_t rem = cnt - (int64_t)i * p.tmax;
-        p.groups[gb + i] = make_int4(tid, (int)(start + (int64_t)i * p.tmax), (int)(rem < p.tmax ? rem : p.tmax), 0);
-      }
+  int64_t running = 0;
+  for (int64_t base = 0; base < p.batch; base += blockDim.x) {
+    const int64_t r = base + tid;
+    const int64_t c = r < p.batch ? p.cnt[r] : 0;
+    int64_t chunk_total = 0;
+    const int64_t incl = block_scan_incl<false>(c, s_warp, &chunk_total);
+    if (r < p.batch) {
+      p.row_ptr[r] = (int32_t)(running + incl - c);
+      p.cursor[r] = (int32_t)(running + incl - c);
     }
-    if (tid == 0) {
-      p.hdr[kHdrErr] = s_err;
-      p.hdr[kHdrGroups] = (uint32_t)n_groups;
-      p.hdr[kHdrCovered] = (uint32_t)covered;
-    }
+    running += chunk_total;
   }
-
-  // ---- token scales: per (group, K-block) a 512-byte chunk in the TMEM-copy layout
-  {
-    const int sub = tid >> 7, i = tid & 127;  // 8 chunks per block iteration, 128 threads each
-    const int64_t items = (int64_t)n_groups * p.KB;
-    const int64_t rowb = 2 * (int64_t)p.Ks;  // bytes per token row of pertoken_scale
-    for (int64_t item = (int64_t)blockIdx.x * 8 + sub; item < items; item += (int64_t)gridDim.x * 8) {
-      const int gidx = (int)(item / p.KB);
-      const int kb = (int)(item % p.KB);
-      int lo = 0, hi = E - 1;  // expert e with s_gbase[e] <= gidx < s_gbase[e+1]
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_gbase[mid] <= gidx) lo = mid; else hi = mid - 1;
-      }
-      const int64_t first = s_start[lo] + (int64_t)(gidx - s_gbase[lo]) * p.tmax;
-      const int64_t rem = (s_end[lo] - s_start[lo]) - (int64_t)(gidx - s_gbase[lo]) * p.tmax;
-      const int64_t T = rem < p.tmax ? rem : p.tmax;
-      uint32_t w = 0x7F7F7F7Fu;
-      if (i < T) {
-        const uint8_t* src = p.pertoken_scale + (first + i) * rowb;
-        w = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int64_t blk = (int64_t)kb * 4 + q;
-          const uint32_t v = (blk * 32 < p.K) ? src[blk] : 127u;
-          w |= v << (8 * q);
-        }
-      }
-      uint8_t* dst = p.tsf + item * kSfChunk;
-      *reinterpret_cast<uint32_t*>(dst + 16 * (i & 31) + 4 * (i >> 5)) = w;
-    }
-  }
-
-  // ---- deterministic mode: CSR of covered tokens by output row (unordered within a row)
-  if (p.deterministic && blockIdx.x == gridDim.x - 1) {
-    for (int64_t r = tid; r < p.batch; r += blockDim.x) p.cnt[r] = 0;
-    __syncthreads();
-    for (int64_t t = tid; t < covered; t += blockDim.x) {
-      const int64_t r = load_row(p.row_index, p.row_i32, t);
-      if (r >= 0 && r < p.batch) atomicAdd(&p.cnt[r], 1);
-    }
-    __syncthreads();
-    int64_t running = 0;
-    for (int64_t base = 0; base < p.batch; base += blockDim.x) {
-      const int64_t r = base + tid;
-      const int64_t c = r < p.batch ? p.cnt[r] : 0;
-      int64_t chunk_total = 0;
-      const int64_t incl = block_scan_incl<false>(c, s_warp, &chunk_total);
-      if (r < p.batch) {
-        p.row_ptr[r] = (int32_t)(running + incl - c);
-        p.cursor[r] = (int32_t)(running + incl - c);
-      }
-      running += chunk_total;
-    }
-    if (tid == 0) p.row_ptr[p.batch] = (int32_t)running;
-    __syncthreads();
-    for (int64_t t = tid; t < covered; t += blockDim.x) {
-      const int64_t r = load_row(p.row_index, p.row_i32, t);
-      if (r >= 0 && r < p.batch) p.sorted[atomicAdd(&p.cursor[r], 1)] = (int32_t)t;
-    }
+  if (tid == 0) p.row_ptr[p.batch] = (int32_t)running;
+  __syncthreads();
+  for (int64_t t = tid; t < covered; t += blockDim.x) {
+    const int64_t r = load_row(p.row_index, p.row_i32, t);
+    if (r >= 0 && r < p.batch) p.sorted[atomicAdd(&p.cursor[r], 1)] = (int32_t)t;
   }
 }
 
-cudaError_t launch_prologue(const PrologueParams& p, int grid, cudaStream_t s) {
-  prologue_kernel<<<grid, 1024, 0, s>>>(p);
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
+  route_kernel<<<1, 1024, 0, s>>>(p);
   return cudaGetLastError();
 }
 

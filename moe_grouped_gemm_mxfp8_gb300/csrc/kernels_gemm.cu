@@ -1,6 +1,6 @@
 // Persistent grouped GEMM of MXFP8 grouped-matmul-finalize-routing on sm_103a.
 //
-// Work: for every token group g (at most TMAX routed tokens of one expert e),
+// Work: for every token group g (at most `tmax` routed tokens of one expert e),
 // every 128-column tile j of the output and every 128-element K block kb,
 //   D[n, t] += sum_{k in block} (x2[e,k,n] * s_w) * (x1[t,k] * s_x)
 // with tcgen05.mma kind::mxf8f6f4 block_scale (one E8M0 scale per 32 K).
@@ -8,14 +8,22 @@
 // N-wide B operand (N = tokens rounded up to 16), so experts holding few tokens
 // still stream each weight byte exactly once.
 //
-// Roles (192 threads, one CTA per SM):
-//   warp 0     TMA producer: prepared weight tile + its scales (one bulk copy),
-//              token rows (16-row tensor-map boxes), token scales (bulk copy)
+// Every CTA first decodes group_list itself (at most 1024 experts) into shared
+// memory: contiguous expert ranges, the token group width tmax in {32, 64, 128}
+// (the smallest that holds the largest expert, so a skewed routing re-reads as
+// few weight tiles as possible), and the first group of every expert.  The
+// shared-memory ring is then cut into as many stages as fit for that width.
+//
+// Roles (224 threads, one CTA per SM):
+//   warp 0     TMA producer: prepared weight tile + its scales (one bulk copy) and
+//              the token rows (boxes of 128, 64, 32 or 16 rows)
 //   warp 1     TMEM owner and MMA issuer (scale copies to TMEM, 4 MMAs per stage)
 //   warps 2-5  epilogue: TMEM -> registers, x logit, red.global.add.f32 into
 //              out[row_index[t], n] (or a plain store into the per-token buffer in
 //              deterministic mode); before the first tile they add the shared
 //              input for their slice of rows.
+//   warp 6     token-scale packer: pertoken_scale bytes of the stage's tokens into
+//              the 32-row x 16-byte layout tcgen05.cp spreads over TMEM lanes.
 //
 // Scheduling: atomic mode splits the total (group, tile, K-block) iteration space
 // evenly over the CTAs (stream-K); a tile cut between CTAs is finished by
@@ -30,23 +38,34 @@
 
 namespace gmmfr {
 
-template <int TMAX>
-struct GemmCfg {
-  static constexpr int kXBytes = TMAX * 128;
-  static constexpr int kOffW = 0;                        // 16384 B weights (1024-aligned)
-  static constexpr int kOffWSF = kWTileBytes;            // 512 B weight scales
-  static constexpr int kOffXSF = kWTileBytes + kSfChunk; // 512 B token scales
-  static constexpr int kOffX = kWTileBytes + 2 * kSfChunk;  // token rows (1024-aligned)
-  static constexpr int kStageBytes = kOffX + kXBytes;
-  static constexpr int kStages = TMAX == 128 ? 6 : (TMAX == 64 ? 8 : 10);
-  static constexpr int kSfCol0 = 2 * TMAX;  // TMEM: 2 accumulators, then 8 scale columns per stage
-  static constexpr int kTmemCols = (2 * TMAX + 8 * kStages) <= 256 ? 256 : 512;
-  static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
-  static_assert(kOffX % 1024 == 0 && kStageBytes % 1024 == 0, "operand tiles must stay 1024-aligned");
-  static_assert(2 * TMAX + 8 * kStages <= kTmemCols, "TMEM budget");
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
-};
+namespace cfg {
+// One ring of stages; a stage holds everything one K block of a segment needs:
+//   [0, 16384)        FP8 weight tile (1024-aligned, 128-byte swizzle)
+//   [16384, 16896)    its E8M0 scales (same bulk copy)
+//   [16896, 17408)    the token scales (packed by warp 6)
+//   [17408, ...)      tmax token rows of 128 bytes (1024-aligned, 128-byte swizzle)
+// Loaded L2 latency is about that of HBM here, so token rows need the same lead
+// time as weights and share the stage.
+constexpr int kMaxStages = 10;
+constexpr int kOffWSF = kWTileBytes;
+constexpr int kOffXSF = kWTileBytes + kSfChunk;
+constexpr int kOffX = kWTileBytes + 2 * kSfChunk;
+__host__ __device__ constexpr int stage_bytes(int tmax) { return kOffX + tmax * 128; }
+__host__ __device__ constexpr int n_stages(int tmax) { return tmax <= 32 ? 10 : (tmax <= 64 ? 8 : 6); }
+constexpr int kArena = 10 * 21504;  // 10 x 21504 (tmax 32), 8 x 25600 (64), 6 x 33792 (128)
+static_assert(n_stages(32) * stage_bytes(32) <= kArena && n_stages(64) * stage_bytes(64) <= kArena &&
+                  n_stages(128) * stage_bytes(128) <= kArena, "ring arena");
+constexpr int kTmemCols = 512;  // 2 x tmax accumulator columns + 8 scale columns per stage
+static_assert(2 * 128 + 8 * 6 <= kTmemCols && 2 * 64 + 8 * 8 <= kTmemCols && 2 * 32 + 8 * 10 <= kTmemCols, "TMEM");
+constexpr int kNumBars = 2 * kMaxStages + 6;
+constexpr int kBarOff = kArena;
+constexpr int kEndOff = kBarOff + kNumBars * 8;              // int32 s_end[1024]
+constexpr int kGbaseOff = kEndOff + 4 * kMaxExperts;         // int32 s_gbase[1025]
+constexpr int kScanOff = kGbaseOff + 4 * (kMaxExperts + 4);  // int64 scan scratch[8]
+constexpr int kMiscOff = kScanOff + 8 * 8;                   // int32 misc[8]
+constexpr int kSmemBytes = kMiscOff + 32 + 1024;             // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+}  // namespace cfg
 
 struct Seg {
   int g, j, kb0, kb1, slot;
@@ -54,7 +73,7 @@ struct Seg {
 
 // The sequence of (group, tile, K range) segments of one CTA; every role walks it.
 // Tiles are ordered column-tile-major (tile = j * n_groups + g), so the token
-// groups of one expert that holds more than TMAX tokens are adjacent and their
+// groups of one expert that holds more than tmax tokens are adjacent and their
 // shared weight tiles are re-read while still in L2.
 struct Sched {
   int64_t i, i_end, step;
@@ -102,9 +121,30 @@ struct Sched {
   }
 };
 
+// Expert ranges and token groups decoded from group_list, in shared memory.
+struct Groups {
+  const int32_t* end;    // end of expert e's token range (ranges are contiguous from 0)
+  const int32_t* gbase;  // first group of expert e; gbase[E] = number of groups
+  int E, tmax;
+  // group g -> expert, first token, tokens
+  __device__ void info(int g, int& e, int& t0, int& T) const {
+    int lo = 0, hi = E - 1;  // largest e with gbase[e] <= g (always a non-empty expert)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (gbase[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    const int start = lo ? end[lo - 1] : 0;
+    const int i = g - gbase[lo];
+    t0 = start + i * tmax;
+    const int rem = end[lo] - t0;
+    T = rem < tmax ? rem : tmax;
+  }
+};
+
 struct Ctl {
   volatile int* abort;
-  uint32_t* err;
+  uint32_t* err;  // shared-memory error bits of this CTA
   int64_t timeout_ns;
 };
 
@@ -124,6 +164,14 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
   }
 }
 
+// wait_bar for a whole warp: every lane waits in hardware (the warp stays
+// converged and sleeps in try_wait), then a vote makes the outcome uniform, so
+// a timeout seen by one lane can never split the warp.
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
+  const bool ok = wait_bar(bar, parity, c);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // Wait used while draining after an abort: ignores the abort flag, fixed 1 s limit.
 __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer();
@@ -139,6 +187,90 @@ __device__ __forceinline__ int load_row32(const void* rows, int row_i32, int64_t
 }
 
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// Block-wide inclusive scan (sum or max) over the kGemmThreads threads; `total`
+// gets the last value.  Every thread must call it.
+template <bool kMax>
+__device__ int64_t cta_scan(int64_t v, int64_t* scratch, int64_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kWarps = kGemmThreads / 32;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = kMax ? (u > v ? u : v) : v + u;
+  }
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  int64_t carry = kMax ? INT64_MIN : 0, all = kMax ? INT64_MIN : 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int64_t u = scratch[w];
+    if (w < warp) carry = kMax ? (u > carry ? u : carry) : carry + u;
+    all = kMax ? (u > all ? u : all) : all + u;
+  }
+  if (warp > 0) v = kMax ? (carry > v ? carry : v) : v + carry;
+  total = all;
+  __syncthreads();
+  return v;
+}
+
+// Expert ranges (MXFP8 grouped_matmul_finalize_routing write-up, section 4.3:
+// type 0 prefix sums, type 1 counts),
+// made contiguous and clamped to [0, M]; sets kErrBadGroupList when clamping was
+// needed.  Fills s_end, chooses tmax, fills s_gbase.  Returns the group count.
+__device__ int decode_groups(const GemmParams& p, int32_t* s_end, int32_t* s_gbase, int64_t* scratch,
+                             uint32_t* s_err, int& tmax_out) {
+  const int E = p.E;
+  const int64_t M = p.M;
+  const int tid = threadIdx.x;
+  int64_t carry = 0;
+  for (int base = 0; base < E; base += kGemmThreads) {  // uniform trip count
+    const int e = base + tid;
+    const int64_t g = e < E ? p.group_list[e] : 0;
+    int64_t v, tot;
+    if (p.group_list_type == 1) {
+      if (e < E && g < 0) atomicOr(s_err, kErrBadGroupList);
+      const int64_t c = e < E ? (g < 0 ? 0 : (g > M ? M + 1 : g)) : 0;
+      v = cta_scan<false>(c, scratch, tot) + carry;
+      carry += tot;
+    } else {
+      const int64_t prev = (e > 0 && e < E) ? p.group_list[e - 1] : 0;
+      if (e < E && (g < prev || g > M)) atomicOr(s_err, kErrBadGroupList);
+      const int64_t c = e < E ? (g < 0 ? 0 : (g > M ? M : g)) : 0;
+      v = cta_scan<true>(c, scratch, tot);
+      v = v > carry ? v : carry;
+      carry = tot > carry ? tot : carry;
+    }
+    if (e < E) s_end[e] = (int32_t)(v < M ? v : M);
+  }
+  if (p.group_list_type == 1 && tid == 0 && carry > M) atomicOr(s_err, kErrBadGroupList);
+  __syncthreads();
+  // largest expert -> token group width
+  int64_t mx = 0;
+  for (int e = tid; e < E; e += kGemmThreads) {
+    const int64_t c = s_end[e] - (e ? s_end[e - 1] : 0);
+    mx = c > mx ? c : mx;
+  }
+  int64_t mx_all;
+  cta_scan<true>(mx, scratch, mx_all);
+  int tmax = mx_all <= 32 ? 32 : (mx_all <= 64 ? 64 : 128);
+  if (p.tmax_fixed) tmax = p.tmax_fixed;
+  // first group of every expert
+  int64_t gcarry = 0;
+  for (int base = 0; base < E; base += kGemmThreads) {
+    const int e = base + tid;
+    const int64_t c = e < E ? s_end[e] - (e ? s_end[e - 1] : 0) : 0;
+    const int64_t ng = (c + tmax - 1) / tmax;
+    int64_t tot;
+    const int64_t incl = cta_scan<false>(ng, scratch, tot) + gcarry;
+    if (e < E) s_gbase[e] = (int32_t)(incl - ng);
+    gcarry += tot;
+  }
+  if (tid == 0) s_gbase[E] = (int32_t)gcarry;
+  __syncthreads();
+  tmax_out = tmax;
+  return (int)gcarry;
+}
 
 // out[offset + i, n] += w * shared[i, n] for this CTA's slice (atomic mode only).
 __device__ void shared_add_slice(const GemmParams& p, int ep_tid) {
@@ -165,27 +297,75 @@ __device__ void shared_add_slice(const GemmParams& p, int ep_tid) {
   }
 }
 
-template <int TMAX>
+// The four E8M0 bytes of token t for the 32-element blocks 4*kb .. 4*kb+3
+// (blocks starting at or past K are padding: 127 = 1.0).
+__device__ __forceinline__ uint32_t token_scale_word(const GemmParams& p, int64_t t, int kb) {
+  const int64_t rowb = 2 * (int64_t)p.Ks;
+  const uint8_t* src = p.pertoken_scale + t * rowb + 4 * kb;
+  if ((rowb & 3) == 0 && (int64_t)(4 * kb + 3) * 32 < p.K) return *reinterpret_cast<const uint32_t*>(src);
+  uint32_t w = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w |= ((int64_t)(4 * kb + q) * 32 < p.K ? (uint32_t)src[q] : 127u) << (8 * q);
+  return w;
+}
+
+// Item iterator of the token-scale packer: one (segment, K block) per stage.
+struct PackIter {
+  Seg sg;
+  int kb, kb1, t0, T;
+  bool valid;
+};
+
+__device__ __forceinline__ bool pack_next(PackIter& it, Sched& sched, const Groups& groups) {
+  if (it.valid && ++it.kb < it.kb1) return true;
+  while (sched.next(it.sg)) {
+    int e;
+    groups.info(it.sg.g, e, it.t0, it.T);
+    it.kb = it.sg.kb0;
+    it.kb1 = it.sg.kb1;
+    if (it.kb < it.kb1) {
+      it.valid = true;
+      return true;
+    }
+  }
+  it.valid = false;
+  return false;
+}
+
+// Scale words of tokens lane, lane+32, lane+64, lane+96 of the item (127 = 1.0 past the group).
+__device__ __forceinline__ void pack_load(const GemmParams& p, const PackIter& it, uint32_t (&w)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = lane + 32 * r;
+    w[r] = (it.valid && i < it.T) ? token_scale_word(p, (int64_t)it.t0 + i, it.kb) : 0x7F7F7F7Fu;
+  }
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmap_x1, const __grid_constant__ GemmParams p) {
-  using C = GemmCfg<TMAX>;
+    gemm_kernel(const __grid_constant__ TokenMaps tmaps, const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
-  uint64_t* full = bars;                      // [kStages] TMA bytes landed
-  uint64_t* empty = bars + C::kStages;        // [kStages] MMAs done reading the stage
-  uint64_t* accf = bars + 2 * C::kStages;     // [2] accumulator ready
-  uint64_t* acce = accf + 2;                  // [2] accumulator drained by the epilogue
-  uint64_t* drain = acce + 2;                 // [1] all MMAs of this CTA complete
-  uint64_t* stall = drain + 1;                // [1] never arrived on (testing aid)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stall + 1);
-  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + cfg::kBarOff);
+  uint64_t* full = bars;                         // [kMaxStages] copies landed + token scales packed
+  uint64_t* empty = bars + cfg::kMaxStages;      // [kMaxStages] MMAs done reading the stage
+  uint64_t* accf = bars + 2 * cfg::kMaxStages;   // [2] accumulator ready
+  uint64_t* acce = accf + 2;                     // [2] accumulator drained by the epilogue
+  uint64_t* drain = acce + 2;                    // [1] all MMAs of this CTA complete
+  uint64_t* stall = drain + 1;                   // [1] never arrived on (testing aid)
+  int32_t* s_end = reinterpret_cast<int32_t*>(smem + cfg::kEndOff);
+  int32_t* s_gbase = reinterpret_cast<int32_t*>(smem + cfg::kGbaseOff);
+  int64_t* s_scan = reinterpret_cast<int64_t*>(smem + cfg::kScanOff);
+  int32_t* misc = reinterpret_cast<int32_t*>(smem + cfg::kMiscOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&misc[0]);
+  int* abort_flag = &misc[1];
+  uint32_t* s_err = reinterpret_cast<uint32_t*>(&misc[2]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
+    for (int s = 0; s < cfg::kMaxStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&full[s]), 2);  // producer (with bytes) + packer
       ptx::mbar_init(ptx::smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -195,20 +375,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ptx::mbar_init(ptx::smem_u32(drain), 1);
     ptx::mbar_init(ptx::smem_u32(stall), 1);
     *abort_flag = 0;
+    *s_err = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) ptx::prefetch_tensormap(&tmap_x1);
+  if (warp == 0 && lane < 4) ptx::prefetch_tensormap(&tmaps.m[lane]);
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), cfg::kTmemCols);
     ptx::tmem_relinquish();
   }
+  __syncthreads();
+  int tmax;
+  const int n_groups = decode_groups(p, s_end, s_gbase, s_scan, s_err, tmax);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const Ctl ctl{abort_flag, p.err, p.timeout_ns};
-  const int n_groups = (int)p.hdr[kHdrGroups];
+  const Groups groups{s_end, s_gbase, p.E, tmax};
+  const int stage_bytes = cfg::stage_bytes(tmax);
+  const int n_stages = cfg::n_stages(tmax);
+  const Ctl ctl{abort_flag, s_err, p.timeout_ns};
   Sched sched;
   sched.init(n_groups, p.NT, p.KB, p.deterministic != 0, p.split);
   const uint32_t smem_base = ptx::smem_u32(smem);
@@ -216,50 +402,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t pol_stream = ptx::l2_evict_first_policy();  // weights: read once
-      const uint64_t pol_keep = ptx::l2_evict_last_policy();     // tokens: reused by every tile
-      int fills[C::kStages];
+      const uint64_t pol_stream = ptx::l2_evict_first_policy();  // weights read once
+      const uint64_t pol_keep = ptx::l2_evict_last_policy();     // tokens (reused by every column tile), and
+                                                                 // weights of experts spanning several groups
+      int fills[cfg::kMaxStages];
 #pragma unroll
-      for (int s = 0; s < C::kStages; ++s) fills[s] = 0;
+      for (int s = 0; s < cfg::kMaxStages; ++s) fills[s] = 0;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       if (p.test_stall) ok = wait_bar(ptx::smem_u32(stall), 0, ctl);
       Seg sg;
       while (ok && sched.next(sg)) {
-        const int4 gr = p.groups[sg.g];
-        const int e = gr.x, t0 = gr.y, T = gr.z;
-        const int nbox = (T + kTokBox - 1) / kTokBox;
-        const uint32_t tx = kPrepTileBytes + kSfChunk + nbox * kTokBox * 128;
+        int e, t0, T;
+        groups.info(sg.g, e, t0, T);
+        const int m = (T + 15) / 16;  // token rows in 16-row units: boxes of 128/64/32/16 rows
+        const uint32_t tx = kPrepTileBytes + m * 16 * 128;
         const uint8_t* wsrc = p.prepared + ((int64_t)e * p.NT + sg.j) * p.KB * (int64_t)kPrepTileBytes;
-        const uint8_t* ssrc = p.tsf + (int64_t)sg.g * p.KB * kSfChunk;
+        // sibling groups of the same expert read the same weight tiles shortly after
+        const uint64_t pol_w = (s_gbase[e + 1] - s_gbase[e]) > 1 ? pol_keep : pol_stream;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (!wait_bar(ptx::smem_u32(&empty[stage]), phase ^ 1, ctl)) {
             ok = false;
             break;
           }
           const uint32_t fb = ptx::smem_u32(&full[stage]);
-          const uint32_t sb = smem_base + stage * C::kStageBytes;
+          const uint32_t sb = smem_base + stage * stage_bytes;
           ptx::mbar_arrive_expect_tx(fb, tx);
-          ptx::bulk_g2s(sb + C::kOffW, wsrc + (int64_t)kb * kPrepTileBytes, kPrepTileBytes, fb, pol_stream);
-          ptx::bulk_g2s(sb + C::kOffXSF, ssrc + (int64_t)kb * kSfChunk, kSfChunk, fb, pol_keep);
-          for (int b = 0; b < nbox; ++b)
-            ptx::tma_load_2d(sb + C::kOffX + b * kTokBox * 128, &tmap_x1, kb * kTileK, t0 + b * kTokBox, fb, pol_keep);
+          ptx::bulk_g2s(sb, wsrc + (int64_t)kb * kPrepTileBytes, kPrepTileBytes, fb, pol_w);
+          // token rows: one 128-row box, or a 64-row box, then 32-row boxes and a
+          // last 16-row box for an odd count (measured fastest on this part)
+          int row = 0;
+          if (m == 8) {
+            ptx::tma_load_2d(sb + cfg::kOffX, &tmaps.m[3], kb * kTileK, t0, fb, pol_keep);
+            row = 128;
+          } else if (m > 4) {
+            ptx::tma_load_2d(sb + cfg::kOffX, &tmaps.m[2], kb * kTileK, t0, fb, pol_keep);
+            row = 64;
+          }
+          for (; row < m * 16; row += 32) {
+            const int last16 = row + 16 == m * 16;
+            ptx::tma_load_2d(sb + cfg::kOffX + row * 128, &tmaps.m[last16 ? 0 : 1], kb * kTileK, t0 + row, fb,
+                             pol_keep);
+          }
           ++fills[stage];
-          if (++stage == C::kStages) {
+          if (++stage == n_stages) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
-      if (ok) {
-        // all fills consumed: wait until the MMA warp has released every stage
-        for (int s = 0; s < C::kStages; ++s)
+      if (ok) {  // all fills consumed: wait until the MMA warp has released every stage
+        for (int s = 0; s < n_stages; ++s)
           if (fills[s] > 0 && !wait_bar(ptx::smem_u32(&empty[s]), (fills[s] - 1) & 1, ctl)) break;
       }
-      if (*abort_flag) {
-        // aborted: let every issued copy land before shared memory is released
-        for (int s = 0; s < C::kStages; ++s)
+      if (*abort_flag) {  // aborted: let every issued copy land before shared memory is released
+        for (int s = 0; s < n_stages; ++s)
           if (fills[s] > 0) wait_bar_drain(ptx::smem_u32(&full[s]), (fills[s] - 1) & 1);
       }
     }
@@ -273,34 +471,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       Seg sg;
       bool ok = true;
       while (ok && sched.next(sg)) {
-        const int T = p.groups[sg.g].z;
+        int e, t0, T;
+        groups.info(sg.g, e, t0, T);
         const uint32_t npad = (uint32_t)((T + 15) / 16) * 16;
         const uint32_t idesc = p.idesc | ((npad >> 3) << 17);
         const int buf = acc_i & 1;
         const uint32_t aph = (acc_i >> 1) & 1;
         if (!wait_bar(ptx::smem_u32(&acce[buf]), aph ^ 1, ctl)) break;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * TMAX;
+        const uint32_t d_tmem = tmem_base + buf * tmax;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (!wait_bar(ptx::smem_u32(&full[stage]), phase, ctl)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sb = smem_base + stage * C::kStageBytes;
-          const uint32_t sfa = tmem_base + C::kSfCol0 + stage * 8;
+          const uint32_t sb = smem_base + stage * stage_bytes;
+          const uint32_t sfa = tmem_base + 2 * tmax + stage * 8;  // per-stage scale columns
           const uint32_t sfb = sfa + 4;
-          ptx::tc_cp_sf(sfa, ptx::smem_desc(sb + C::kOffWSF, 0, 128, ptx::kSwizzleNone));
-          ptx::tc_cp_sf(sfb, ptx::smem_desc(sb + C::kOffXSF, 0, 128, ptx::kSwizzleNone));
+          ptx::tc_cp_sf(sfa, ptx::smem_desc(sb + cfg::kOffWSF, 0, 128, ptx::kSwizzleNone));
+          ptx::tc_cp_sf(sfb, ptx::smem_desc(sb + cfg::kOffXSF, 0, 128, ptx::kSwizzleNone));
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint64_t adesc = ptx::smem_desc(sb + C::kOffW + 32 * q, 16, 1024, ptx::kSwizzle128B);
-            const uint64_t bdesc = ptx::smem_desc(sb + C::kOffX + 32 * q, 16, 1024, ptx::kSwizzle128B);
+            const uint64_t adesc = ptx::smem_desc(sb + 32 * q, 16, 1024, ptx::kSwizzle128B);
+            const uint64_t bdesc = ptx::smem_desc(sb + cfg::kOffX + 32 * q, 16, 1024, ptx::kSwizzle128B);
             const uint32_t id = idesc | ((uint32_t)q << 4) | ((uint32_t)q << 29);
             ptx::tc_mma_mxf8(d_tmem, adesc, bdesc, id, sfa, sfb, (kb > sg.kb0 || q > 0) ? 1u : 0u);
           }
           ptx::tc_commit(ptx::smem_u32(&empty[stage]));
-          if (++stage == C::kStages) {
+          if (++stage == n_stages) {
             stage = 0;
             phase ^= 1;
           }
@@ -314,6 +513,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       wait_bar_drain(ptx::smem_u32(drain), 0);
     }
     __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ token-scale packer
+    // Walks the (segment, K block) items in stage order; an item's scale words
+    // are loaded three items before its stage is filled, so L2 latency overlaps
+    // the ring.
+    PackIter it;
+    it.valid = false;
+    uint32_t w0[4], w1[4], w2[4];
+    bool v0 = pack_next(it, sched, groups);
+    pack_load(p, it, w0);
+    bool v1 = v0 && pack_next(it, sched, groups);
+    pack_load(p, it, w1);
+    bool v2 = v1 && pack_next(it, sched, groups);
+    pack_load(p, it, w2);
+    int stage = 0;
+    uint32_t phase = 0;
+    while (v0) {
+      if (!warp_wait_bar(ptx::smem_u32(&empty[stage]), phase ^ 1, ctl)) break;
+      uint8_t* xsf = smem + stage * stage_bytes + cfg::kOffXSF;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t*>(xsf + 16 * lane + 4 * r) = w0[r];
+      ptx::fence_proxy_async_smem();  // make the generic-proxy stores visible to tcgen05.cp
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&full[stage]));
+      if (++stage == n_stages) {
+        stage = 0;
+        phase ^= 1;
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        w0[r] = w1[r];
+        w1[r] = w2[r];
+      }
+      v0 = v1;
+      v1 = v2;
+      v2 = v2 && pack_next(it, sched, groups);
+      pack_load(p, it, w2);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
@@ -321,17 +558,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (!p.deterministic && p.shared != nullptr && p.shared_rows > 0 && p.N > 0) shared_add_slice(p, ep_tid);
     int acc_i = 0;
     Seg sg;
+    bool bad_row = false;
     while (sched.next(sg)) {
-      const int4 gr = p.groups[sg.g];
-      const int t0 = gr.y, T = gr.z;
+      int e, t0, T;
+      groups.info(sg.g, e, t0, T);
       const int buf = acc_i & 1;
       const uint32_t aph = (acc_i >> 1) & 1;
-      if (!wait_bar(ptx::smem_u32(&accf[buf]), aph, ctl)) break;
+      if (!warp_wait_bar(ptx::smem_u32(&accf[buf]), aph, ctl)) break;
       ptx::tc_fence_after();
       const int64_t n = (int64_t)sg.j * kTileN + q * 32 + lane;
       const bool n_ok = n < p.N;
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TMAX;
-      bool bad_row = false;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * tmax;
       for (int c0 = 0; c0 < T; c0 += 32) {
         const int tok = c0 + lane;
         int my_row = -1;
@@ -366,49 +603,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      if (bad_row) atomicOr(p.err, kErrBadRowIndex);
       ++acc_i;
     }
+    if (bad_row) atomicOr(s_err, kErrBadRowIndex);
   }
 
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+    ptx::tmem_dealloc(tmem_base, cfg::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    p.hdr[1 + blockIdx.x] = *s_err;
+    if (blockIdx.x == 0) p.hdr[0] = gridDim.x;
   }
 }
 
-int gemm_smem_bytes(int tmax) {
-  switch (tmax) {
-    case 32: return GemmCfg<32>::kSmemBytes;
-    case 64: return GemmCfg<64>::kSmemBytes;
-    default: return GemmCfg<128>::kSmemBytes;
-  }
-}
+int gemm_smem_bytes() { return cfg::kSmemBytes; }
 
-template <int TMAX>
-static cudaError_t launch_t(const CUtensorMap& tmap, const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_gemm(const TokenMaps& tmaps, const GemmParams& p, int grid, cudaStream_t s) {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<TMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         GemmCfg<TMAX>::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gemm_kernel<TMAX><<<grid, kGemmThreads, GemmCfg<TMAX>::kSmemBytes, s>>>(tmap, p);
+  gemm_kernel<<<grid, kGemmThreads, cfg::kSmemBytes, s>>>(tmaps, p);
   return cudaGetLastError();
-}
-
-cudaError_t launch_gemm(const CUtensorMap& tmap, const GemmParams& p, int tmax, int grid, cudaStream_t s) {
-  switch (tmax) {
-    case 32: return launch_t<32>(tmap, p, grid, s);
-    case 64: return launch_t<64>(tmap, p, grid, s);
-    case 128: return launch_t<128>(tmap, p, grid, s);
-    default: return cudaErrorInvalidValue;
-  }
 }
 
 }  // namespace gmmfr

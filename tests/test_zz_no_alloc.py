@@ -66,11 +66,15 @@ def test_static_scratch_matches_workspace_entry_point(deterministic):
 
 
 def test_static_scratch_refuses_oversized_problems():
-    big = B.make_problem(M=1 << 20, K=7168, N=4096, E=1024, batch=1 << 17)
+    # Deterministic mode keeps one FP32 partial per (token, column): 4096 x 4096 x 4 B = 64 MiB,
+    # beyond the 16 MiB scratch.  Every tensor pointer is NULL, so even a call that got past
+    # the size check would be refused by host validation before anything is enqueued.
+    big = B.make_problem(M=4096, K=7168, N=4096, E=256, batch=512, deterministic=True)
+    assert B.gmmfr_workspace_size(big, True) > 16 << 20
     with pytest.raises(B.GmmfrError) as ei:
-        B.gmmfr_grouped_matmul_finalize_routing_static_scratch(big, 256, 256, 256, 256, 256, None, 256, 256)
+        B.gmmfr_grouped_matmul_finalize_routing_static_scratch(big, None, None, None, None, None, None, None, 256)
     assert ei.value.status == B.ERR_WORKSPACE and "16 MiB" in str(ei.value)
     small = B.make_problem(M=16, K=128, N=128, E=1, batch=16)
     with pytest.raises(B.GmmfrError) as ei:
-        B.gmmfr_grouped_matmul_finalize_routing_static_scratch(small, 256, 256, 256, 256, 256, None, 256, None)
+        B.gmmfr_grouped_matmul_finalize_routing_static_scratch(small, None, None, None, None, None, None, None, None)
     assert ei.value.status == B.ERR_INVALID_ARG and "gmmfr_prepare_weights" in str(ei.value)
