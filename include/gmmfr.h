@@ -83,6 +83,10 @@ typedef enum { GMMFR_INDEX_I64 = 0, GMMFR_INDEX_I32 = 1 } gmmfr_index_type;
  *   shared_offset            first out row of the shared add; 0 <= offset, offset + rows <= batch
  *   shared_weight            multiplier of shared_input (default 1.0 on the page)
  *   flags                    GMMFR_DETERMINISTIC or 0
+ *   expected_tokens_per_expert  tiling hint (aclnn V3 tuningConfigOptional, first value: the
+ *                            expected tokens per expert); 0 = none.  When > 0 it fixes the
+ *                            token group width (32, 64 or 128, the smallest that holds it)
+ *                            instead of deriving it from the largest expert on the device.
  */
 typedef struct {
   int64_t M, K, N, E, batch;
@@ -95,6 +99,7 @@ typedef struct {
   int64_t shared_offset;
   float shared_weight;
   uint32_t flags;
+  int64_t expected_tokens_per_expert;
 } gmmfr_problem;
 
 /*
@@ -136,6 +141,9 @@ GMMFR_API gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int ha
  *   logit           [M] float32, or NULL for weight 1 (has_logit = False)
  *   row_index       [M] int64 or int32; values in [0,batch), checked on the device
  *   shared_input    [shared_rows,N] bfloat16, or NULL when shared_rows == 0
+ *   bias            [E,N] bfloat16 (aclnn V3 biasOptional, BF16 on the MX path), or NULL;
+ *                   read as a per-expert, per-column term added to the matmul result
+ *                   before the logit weighting: out[r,n] += logit * (mm(t,n) + bias[e,n])
  *   out             [batch,N] float32, read and accumulated into in place
  *   prepared        output of gmmfr_prepare_weights for the same x2/scale, or NULL
  *   workspace       at least gmmfr_workspace_size bytes, 256-byte aligned; its
@@ -152,7 +160,7 @@ GMMFR_API gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int ha
 GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing(
     const gmmfr_problem* problem, const void* x1, const void* x2, const void* scale,
     const void* pertoken_scale, const int64_t* group_list, const float* logit,
-    const void* row_index, const void* shared_input, float* out, const void* prepared,
+    const void* row_index, const void* shared_input, const void* bias, float* out, const void* prepared,
     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
@@ -170,7 +178,7 @@ GMMFR_API gmmfr_status gmmfr_check_device_errors(const void* workspace, void* st
  * memory pool owns the whole device and forbids outside allocations, serving
  * loops where a cudaMalloc (which can synchronise the device and fail under
  * memory pressure) is not acceptable, or plain C callers without an allocator.
- * This call takes the same tensors as the operator minus x2, scale and the
+ * This call takes the same tensors as the operator minus x2, scale, bias and the
  * workspace, and uses instead a 16 MiB scratch array compiled into the library
  * as a file-scope __device__ variable.  Every GPU that loads the library holds
  * those 16 MiB until the process exits.  It calls no cudaMalloc / cudaFree.

@@ -42,6 +42,7 @@ class Problem(ctypes.Structure):
         ("group_list_type", ctypes.c_int32), ("row_index_type", ctypes.c_int32),
         ("shared_rows", ctypes.c_int64), ("shared_offset", ctypes.c_int64),
         ("shared_weight", ctypes.c_float), ("flags", ctypes.c_uint32),
+        ("expected_tokens_per_expert", ctypes.c_int64),
     ]
 
 
@@ -68,7 +69,7 @@ def load(path: str = LIB_PATH):
             lib.gmmfr_prepared_weights_size.argtypes = [P, ctypes.POINTER(sz)]
             lib.gmmfr_prepare_weights.argtypes = [P, vp, vp, vp, sz, vp]
             lib.gmmfr_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
-            lib.gmmfr_grouped_matmul_finalize_routing.argtypes = [P] + [vp] * 11 + [sz, vp]
+            lib.gmmfr_grouped_matmul_finalize_routing.argtypes = [P] + [vp] * 12 + [sz, vp]
             lib.gmmfr_grouped_matmul_finalize_routing_static_scratch.argtypes = [P] + [vp] * 9
             lib.gmmfr_check_device_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
             lib.gmmfr_last_error.restype = ctypes.c_char_p
@@ -93,12 +94,14 @@ def _check(status: int) -> None:
 
 def make_problem(*, M, K, N, E, batch, x1_format=E4M3, x2_format=E4M3, transpose_x2=False,
                  scale_per_expert=False, group_list_type=1, row_index_type=INDEX_I64, shared_rows=0,
-                 shared_offset=0, shared_weight=1.0, deterministic=False) -> Problem:
+                 shared_offset=0, shared_weight=1.0, deterministic=False,
+                 expected_tokens_per_expert=0) -> Problem:
     return Problem(M=M, K=K, N=N, E=E, batch=batch, x1_format=x1_format, x2_format=x2_format,
                    transpose_x2=int(bool(transpose_x2)), scale_per_expert=int(bool(scale_per_expert)),
                    group_list_type=group_list_type, row_index_type=row_index_type,
                    shared_rows=shared_rows, shared_offset=shared_offset, shared_weight=shared_weight,
-                   flags=DETERMINISTIC if deterministic else 0)
+                   flags=DETERMINISTIC if deterministic else 0,
+                   expected_tokens_per_expert=expected_tokens_per_expert)
 
 
 def problem_from_spec(spec, deterministic: bool = False, row_index_type: int = INDEX_I64) -> Problem:
@@ -129,11 +132,11 @@ def gmmfr_workspace_size(problem: Problem, have_prepared: bool) -> int:
 
 
 def gmmfr_grouped_matmul_finalize_routing(problem: Problem, x1, x2, scale, pertoken_scale, group_list, logit,
-                                          row_index, shared_input, out, prepared, workspace, workspace_bytes,
+                                          row_index, shared_input, bias, out, prepared, workspace, workspace_bytes,
                                           stream=None) -> None:
     _check(load().gmmfr_grouped_matmul_finalize_routing(
         ctypes.byref(problem), x1, x2, scale, pertoken_scale, group_list, logit, row_index, shared_input,
-        out, prepared, workspace, workspace_bytes, stream))
+        bias, out, prepared, workspace, workspace_bytes, stream))
 
 
 def gmmfr_grouped_matmul_finalize_routing_static_scratch(problem: Problem, x1, pertoken_scale, group_list, logit,
@@ -209,5 +212,6 @@ def run(problem: Problem, inputs: dict, out, prepared=None, ws=None, stream=None
         problem, _ptr(inputs["x1"]), _ptr(inputs["x2"]) if prepared is None else None,
         _ptr(inputs["scale"]) if prepared is None else None, _ptr(inputs["pertoken_scale"]),
         _ptr(inputs["group_list"]), _ptr(inputs.get("logit")), _ptr(inputs["row_index"]),
-        _ptr(inputs.get("shared_input")), _ptr(out), _ptr(prepared), _ptr(ws), ws.numel(), _stream(stream))
+        _ptr(inputs.get("shared_input")), _ptr(inputs.get("bias")), _ptr(out), _ptr(prepared), _ptr(ws),
+        ws.numel(), _stream(stream))
     return ws

@@ -57,6 +57,8 @@ gmmfr_status validate(const gmmfr_problem* p) {
     return fail(GMMFR_ERR_INVALID_ARG, "shared_offset + shared_rows = %lld exceeds batch = %lld",
                 (long long)(p->shared_offset + p->shared_rows), (long long)p->batch);
   if (p->flags & ~GMMFR_DETERMINISTIC) return fail(GMMFR_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
+  if (p->expected_tokens_per_expert < 0)
+    return fail(GMMFR_ERR_INVALID_ARG, "expected_tokens_per_expert=%lld is negative", (long long)p->expected_tokens_per_expert);
   if (p->K % 16 != 0) return fail(GMMFR_ERR_UNSUPPORTED, "K=%lld: this build needs K %% 16 == 0 (x1 rows are moved by TMA)", (long long)p->K);
   return GMMFR_OK;
 }
@@ -217,7 +219,8 @@ gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const void* x2,
 gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem, const void* x1, const void* x2,
                                                    const void* scale, const void* pertoken_scale,
                                                    const int64_t* group_list, const float* logit,
-                                                   const void* row_index, const void* shared_input, float* out,
+                                                   const void* row_index, const void* shared_input,
+                                                   const void* bias, float* out,
                                                    const void* prepared, void* workspace, size_t workspace_bytes,
                                                    void* stream) {
   if (gmmfr_status st = validate(problem)) return st;
@@ -233,7 +236,8 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   if (x1 && !aligned(x1, 16)) return fail(GMMFR_ERR_INVALID_ARG, "x1 must be 16-byte aligned");
   if (prepared && !aligned(prepared, 16)) return fail(GMMFR_ERR_INVALID_ARG, "prepared must be 16-byte aligned");
   if (!aligned(group_list, 8) || (row_index && !aligned(row_index, p.row_index_type == GMMFR_INDEX_I32 ? 4 : 8)) ||
-      (logit && !aligned(logit, 4)) || (out && !aligned(out, 4)) || (shared_input && !aligned(shared_input, 2)))
+      (logit && !aligned(logit, 4)) || (out && !aligned(out, 4)) || (shared_input && !aligned(shared_input, 2)) ||
+      (bias && !aligned(bias, 2)))
     return fail(GMMFR_ERR_INVALID_ARG, "an input is not aligned to its element size");
   const Layout L = make_layout(problem, prepared != nullptr);
   if (!workspace) return fail(GMMFR_ERR_WORKSPACE, "workspace is NULL (needs %zu bytes)", L.total);
@@ -304,6 +308,7 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   gp.logit = logit;
   gp.row_index = row_index;
   gp.shared = static_cast<const uint16_t*>(shared_input);
+  gp.bias = static_cast<const uint16_t*>(bias);
   gp.out = out;
   gp.ybuf = det ? reinterpret_cast<float*>(ws + L.off_y) : nullptr;
   gp.M = p.M;
@@ -319,6 +324,8 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   gp.KB = (int32_t)L.KB;
   gp.Ks = (int32_t)L.Ks;
   gp.tmax_fixed = fixed_tmax();
+  if (!gp.tmax_fixed && p.expected_tokens_per_expert > 0)
+    gp.tmax_fixed = p.expected_tokens_per_expert <= 32 ? 32 : (p.expected_tokens_per_expert <= 64 ? 64 : 128);
   gp.split = L.split;
   gp.deterministic = det;
   gp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;

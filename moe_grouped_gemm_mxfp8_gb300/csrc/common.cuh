@@ -57,6 +57,7 @@ struct GemmParams {
   const float* logit;
   const void* row_index;
   const uint16_t* shared;  // bf16 bits; added here only in atomic mode
+  const uint16_t* bias;    // [E, N] bf16 bits or null
   float* out;
   float* ybuf;             // deterministic: [split][M][N]
   uint32_t* hdr;           // error slots (see kHdrBytes)

@@ -18,7 +18,7 @@
 //   warp 0     TMA producer: prepared weight tile + its scales (one bulk copy) and
 //              the token rows (boxes of 128, 64, 32 or 16 rows)
 //   warp 1     TMEM owner and MMA issuer (scale copies to TMEM, 4 MMAs per stage)
-//   warps 2-5  epilogue: TMEM -> registers, x logit, red.global.add.f32 into
+//   warps 2-5  epilogue: TMEM -> registers, + bias, x logit, red.global.add.f32 into
 //              out[row_index[t], n] (or a plain store into the per-token buffer in
 //              deterministic mode); before the first tile they add the shared
 //              input for their slice of rows.
@@ -568,6 +568,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ptx::tc_fence_after();
       const int64_t n = (int64_t)sg.j * kTileN + q * 32 + lane;
       const bool n_ok = n < p.N;
+      // the bias term is added once per (token, column): by the segment holding K block 0
+      const float bias_n = (p.bias != nullptr && sg.kb0 == 0 && n_ok) ? bf16f(p.bias[(int64_t)e * p.N + n]) : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * tmax;
       for (int c0 = 0; c0 < T; c0 += 32) {
         const int tok = c0 + lane;
@@ -592,7 +594,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (jj < cnt) {
             const int row = __shfl_sync(0xffffffffu, my_row, jj);
             const float lg = __shfl_sync(0xffffffffu, my_lg, jj);
-            const float val = __uint_as_float(v[jj]) * lg;
+            const float val = (__uint_as_float(v[jj]) + bias_n) * lg;
             if (n_ok) {
               if (p.deterministic) {
                 p.ybuf[((int64_t)sg.slot * p.M + t0 + c0 + jj) * p.N + n] = val;

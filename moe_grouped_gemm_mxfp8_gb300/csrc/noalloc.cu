@@ -61,6 +61,6 @@ extern "C" GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing_static_s
   // The operator overwrites every scratch word it reads (header, group table,
   // token scales, CSR) before reading it, so nothing has to be cleared here.
   return gmmfr_grouped_matmul_finalize_routing(problem, x1, nullptr, nullptr, pertoken_scale, group_list, logit,
-                                               row_index, shared_input, out, prepared, scratch,
+                                               row_index, shared_input, nullptr, out, prepared, scratch,
                                                kStaticScratchBytes, stream);
 }

@@ -71,6 +71,7 @@ class Spec:
     shared_offset: int = 0
     shared_weight: float = 1.0
     out_init: str = "zeros"  # "zeros" | "randn"
+    bias: bool = False       # per-expert, per-column bf16 bias [E, N] (randn)
     seed: int = 0
 
     @property
@@ -180,8 +181,9 @@ def make_inputs(spec: Spec, device: str = "cpu", weights_device: Optional[str] =
     else:
         raise ValueError(spec.out_init)
 
+    bias = torch.randn((E, N), generator=g, dtype=torch.float32).to(torch.bfloat16) if spec.bias else None
     d = dict(x1=x1, x2=x2, scale=scale, pertoken_scale=pertoken_scale, group_list=group_list,
-             logit=logit, row_index=row_index, shared_input=shared_input, out=out)
+             logit=logit, row_index=row_index, shared_input=shared_input, out=out, bias=bias)
     if device != "cpu":
         d = {k: (v.to(device) if v is not None else None) for k, v in d.items()}
     return d

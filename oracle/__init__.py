@@ -52,7 +52,7 @@ class _Args(ctypes.Structure):
         ("logit", ctypes.c_void_p), ("row_index", ctypes.c_void_p),
         ("shared_input", ctypes.c_void_p), ("shared_rows", ctypes.c_int64),
         ("shared_offset", ctypes.c_int64), ("shared_weight", ctypes.c_double),
-        ("out_init", ctypes.c_void_p),
+        ("out_init", ctypes.c_void_p), ("bias", ctypes.c_void_p),
     ]
 
 
@@ -103,12 +103,12 @@ class Problem:
     def __init__(self, *, M, K, N, E, batch, x1, x2, scale, pertoken_scale, group_list,
                  row_index, out, x1_dtype=0, x2_dtype=0, transpose_x2=False,
                  scale_per_expert=False, group_list_type=1, logit=None, shared_input=None,
-                 shared_offset=0, shared_weight=1.0):
+                 shared_offset=0, shared_weight=1.0, bias=None):
         self.keep = dict(
             x1=_np(x1, np.uint8), x2=_np(x2, np.uint8), scale=_np(scale, np.uint8),
             pts=_np(pertoken_scale, np.uint8), gl=_np(group_list, np.int64),
             logit=_np(logit, np.float32), rows=_np(row_index, np.int64),
-            shared=_np(shared_input, np.uint16), out=_np(out, np.float32))
+            shared=_np(shared_input, np.uint16), out=_np(out, np.float32), bias=_np(bias, np.uint16))
         k = self.keep
         assert k["x1"].size == M * K and k["x2"].size == E * K * N
         assert k["out"].size == batch * N and k["rows"].size == M and k["gl"].size == E
@@ -124,7 +124,7 @@ class Problem:
             x1=ptr(k["x1"]), x2=ptr(k["x2"]), scale=ptr(k["scale"]), pertoken_scale=ptr(k["pts"]),
             group_list=ptr(k["gl"]), logit=ptr(k["logit"]), row_index=ptr(k["rows"]),
             shared_input=ptr(k["shared"]), shared_rows=shared_rows, shared_offset=int(shared_offset),
-            shared_weight=float(shared_weight), out_init=ptr(k["out"]))
+            shared_weight=float(shared_weight), out_init=ptr(k["out"]), bias=ptr(k["bias"]))
         self.batch, self.N, self.E = batch, N, E
 
 
@@ -137,7 +137,8 @@ def problem_from_spec(spec, inputs) -> Problem:
                    x2_dtype=spec.x2_dtype, transpose_x2=spec.transpose_x2,
                    scale_per_expert=spec.scale_per_expert, group_list_type=spec.group_list_type,
                    logit=inputs["logit"], shared_input=inputs["shared_input"],
-                   shared_offset=spec.shared_offset, shared_weight=spec.shared_weight)
+                   shared_offset=spec.shared_offset, shared_weight=spec.shared_weight,
+                   bias=inputs.get("bias"))
 
 
 def run(p: Problem) -> Tuple[np.ndarray, np.ndarray, int]:

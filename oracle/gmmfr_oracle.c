@@ -31,6 +31,9 @@
  *     start_e, M); an input that needs clamping raises ORACLE_BAD_GROUP_LIST;
  *   - a token whose row_index is outside [0, batch) contributes nothing and
  *     raises ORACLE_BAD_ROW_INDEX;
+ *   - bias (aclnn V3 biasOptional, BF16 on the MX path; the pages give no formula)
+ *     is read as a per-expert, per-column term added to acc(t,n) before the logit
+ *     weighting: out[row_index[t], n] += logit[t] * (acc(t,n) + bias[e,n]);
  *   - logit == NULL means weight 1 (has_logit=False, section 5.3);
  *     shared_input == NULL skips stage 4;
  *   - contributions are added in ascending token order, the shared term last
@@ -211,8 +214,9 @@ int oracle_gmmfr(const oracle_args* a, double* out64, double* absb) {
           }
         }
         for (int64_t j = 0; j < nn; ++j) {
-          out64[r * N + n0 + j] += lg * acc[j];
-          absb[r * N + n0 + j] += fabs(lg) * ab[j];
+          const double b = a->bias ? oracle_decode_bf16(a->bias[e * N + n0 + j]) : 0.0;
+          out64[r * N + n0 + j] += lg * (acc[j] + b);
+          absb[r * N + n0 + j] += fabs(lg) * (ab[j] + fabs(b));
         }
       }
       free(w);
@@ -256,8 +260,9 @@ int oracle_gmmfr_sampled(const oracle_args* a, int64_t n_samples, const int64_t*
           acc += p;
           ab += fabs(p);
         }
-        v += lg * acc;
-        bnd += fabs(lg) * ab;
+        const double b = a->bias ? oracle_decode_bf16(a->bias[e * N + n]) : 0.0;
+        v += lg * (acc + b);
+        bnd += fabs(lg) * (ab + fabs(b));
       }
     }
     if (a->shared_input && r >= a->shared_offset && r < a->shared_offset + a->shared_rows)

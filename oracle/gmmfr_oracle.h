@@ -44,6 +44,7 @@ typedef struct {
   int64_t shared_offset;
   double shared_weight;
   const float* out_init;         /* [batch,N] */
+  const uint16_t* bias;          /* [E,N] bf16 bits, or NULL */
 } oracle_args;
 
 /* Decoders of single codes, exposed so the tests can pin them. */

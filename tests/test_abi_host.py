@@ -42,8 +42,8 @@ def test_library_exports_every_declared_entry_point(lib):
 
 
 def test_problem_struct_matches_header(lib):
-    # sizeof(gmmfr_problem): 5 int64 + 6 int32 + 2 int64 + float + uint32
-    assert ctypes.sizeof(B.Problem) == 5 * 8 + 6 * 4 + 2 * 8 + 4 + 4
+    # sizeof(gmmfr_problem): 5 int64 + 6 int32 + 2 int64 + float + uint32 + int64
+    assert ctypes.sizeof(B.Problem) == 5 * 8 + 6 * 4 + 2 * 8 + 4 + 4 + 8
 
 
 def _ok_problem(**kw):
@@ -67,6 +67,7 @@ BAD = [
     (dict(shared_offset=1), B.ERR_INVALID_ARG, "exceeds batch"),
     (dict(shared_rows=65), B.ERR_INVALID_ARG, "exceeds batch"),
     (dict(K=5128), B.ERR_UNSUPPORTED, "K % 16"),
+    (dict(expected_tokens_per_expert=-1), B.ERR_INVALID_ARG, "expected_tokens_per_expert"),
 ]
 
 
@@ -78,7 +79,7 @@ def test_invalid_problems_are_rejected_on_the_host(lib, kw, status, msg):
     assert ei.value.status == status and msg in str(ei.value)
     # the operator itself rejects the same problem before enqueuing anything
     with pytest.raises(B.GmmfrError) as ei:
-        B.gmmfr_grouped_matmul_finalize_routing(p, 16, None, None, 16, 16, None, 16, 16, 16, 16, 256, 1 << 30)
+        B.gmmfr_grouped_matmul_finalize_routing(p, 16, None, None, 16, 16, None, 16, 16, None, 16, 16, 256, 1 << 30)
     assert ei.value.status == status
 
 
@@ -111,7 +112,7 @@ def test_bad_pointers_are_rejected_on_the_host(lib, args, msg):
     a.update(args)
     with pytest.raises(B.GmmfrError) as ei:
         B.gmmfr_grouped_matmul_finalize_routing(p, a["x1"], None, None, a["pts"], a["gl"], a["logit"], a["rows"],
-                                                a["shared"], a["out"], a["prepared"], a["ws"], a["ws_bytes"])
+                                                a["shared"], None, a["out"], a["prepared"], a["ws"], a["ws_bytes"])
     assert msg in str(ei.value)
     assert ei.value.status in (B.ERR_INVALID_ARG, B.ERR_WORKSPACE)
 
@@ -119,7 +120,7 @@ def test_bad_pointers_are_rejected_on_the_host(lib, args, msg):
 def test_empty_problems_are_no_ops(lib):
     # N = 0 (aclnn: "x2 supports an empty tensor with N = 0"): nothing to enqueue
     B.gmmfr_grouped_matmul_finalize_routing(_ok_problem(N=0), None, None, None, None, 256, None, None, None,
-                                            None, None, None, 0)
+                                            None, None, None, None, 0)
 
 
 def test_sizes_follow_the_tiling(lib):

@@ -152,6 +152,10 @@ SMALL = {
     "straddle": dict(E=9, M=1344, batch=200, N=256, K=128, rows="random",
                      counts="explicit", explicit_counts=(63, 64, 65, 127, 128, 129, 255, 256, 257)),
     "many_experts": dict(E=300, M=900, batch=300, N=128, K=128, counts="multinomial", rows="random"),
+    # bias: added once per (token, column) even when a tile's K range is split over CTAs
+    "bias_split_k": dict(E=4, M=60, N=320, K=1024, bias=True, rows="random", out_init="randn"),
+    "bias_wide": dict(E=3, M=300, batch=64, N=256, K=256, bias=True, counts="explicit",
+                      explicit_counts=(150, 0, 150), rows="random", transpose_x2=True),
 }
 
 
@@ -160,7 +164,8 @@ def test_small_atomic(name):
     check_full(_spec(**SMALL[name]), W.make_inputs(_spec(**SMALL[name])))
 
 
-@pytest.mark.parametrize("name", ["basic", "transposed", "ragged_counts", "random_rows_shared", "straddle", "k96"])
+@pytest.mark.parametrize("name", ["basic", "transposed", "ragged_counts", "random_rows_shared", "straddle", "k96",
+                                  "bias_split_k"])
 def test_small_deterministic(name):
     spec = _spec(**SMALL[name])
     inp = W.make_inputs(spec)
@@ -174,6 +179,24 @@ def test_token_group_widths(tmax, monkeypatch):
     monkeypatch.setenv("GMMFR_TMAX", tmax)
     spec = _spec(**SMALL["straddle"])
     check_full(spec, W.make_inputs(spec))
+
+
+@pytest.mark.parametrize("hint", [8, 50, 200])
+def test_expected_tokens_hint(hint):
+    """The tiling hint changes the token group width, never the result."""
+    spec = _spec(**SMALL["straddle"])
+    inp = W.make_inputs(spec)
+    d = _dev(inp)
+    prob = B.problem_from_spec(spec)
+    prob.expected_tokens_per_expert = hint
+    prep = B.prepare_weights(prob, d["x2"], d["scale"])
+    out = d["out"].clone()
+    ws = B.run(prob, d, out, prepared=prep)
+    bits = B.gmmfr_check_device_errors(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    ref, absb, flags = oracle.run(oracle.problem_from_spec(spec, inp))
+    init, sh = _extra_terms(spec, inp)
+    assert_close(out.cpu().numpy().astype(np.float64), ref, oracle.tolerance(ref, absb, init, sh))
+    assert bits == flags
 
 
 def test_int32_row_index_and_raw_weights():

@@ -113,6 +113,8 @@ def _torch_golden(spec: W.Spec, inp) -> np.ndarray:
         if c == 0:
             continue
         mm = a[start:start + c] @ b[e]
+        if inp.get("bias") is not None:  # bias reading: added per expert and column before the logit
+            mm = mm + inp["bias"][e].to(torch.float64)[None, :]
         if inp["logit"] is not None:
             mm = mm * inp["logit"][start:start + c].to(torch.float64)[:, None]
         out.index_add_(0, inp["row_index"][start:start + c], mm)
@@ -238,6 +240,8 @@ TINY = [
     dict(counts="explicit", explicit_counts=(0, 5, 0), M=9),     # zero-token experts, tokens past the groups
     dict(rows="random", shared_rows=2, shared_offset=1, shared_weight=0.7, out_init="randn"),
     dict(logit="none", shared_rows=0),
+    dict(bias=True, rows="random", out_init="randn"),
+    dict(bias=True, transpose_x2=True, counts="explicit", explicit_counts=(0, 7, 5), M=14),
 ]
 
 
@@ -358,8 +362,27 @@ def test_k_tail_padding_scale_is_ignored():
     assert np.array_equal(out, out2)
 
 
+def test_bias_closed_form():
+    """Zero activations leave only the bias: out[r,n] = init + sum over the row's
+    tokens of logit * bias[expert, n] (bf16 values chosen exactly representable)."""
+    spec = _spec(bias=True, rows="mod", batch=12, shared_rows=0, out_init="randn")
+    inp = W.make_inputs(spec)
+    inp["x1"].zero_()
+    bias = torch.tensor([[0.5 * (e + 1) - 0.25 * (n % 5) for n in range(spec.N)] for e in range(spec.E)])
+    inp["bias"] = bias.to(torch.bfloat16)
+    out, absb, _ = _run(spec, inp)
+    exp = inp["out"].numpy().astype(np.float64).copy()
+    counts = inp["group_list"].tolist()
+    t = 0
+    for e, c in enumerate(counts):
+        for _ in range(c):
+            exp[int(inp["row_index"][t])] += float(inp["logit"][t]) * bias[e].double().numpy()
+            t += 1
+    np.testing.assert_allclose(out, exp, rtol=0, atol=1e-12)
+
+
 def test_sampled_equals_full():
-    spec = _spec(rows="random", out_init="randn", shared_rows=3, shared_offset=1)
+    spec = _spec(rows="random", out_init="randn", shared_rows=3, shared_offset=1, bias=True)
     inp = W.make_inputs(spec)
     p = oracle.problem_from_spec(spec, inp)
     out, absb, _ = oracle.run(p)
