@@ -247,3 +247,58 @@ def flops(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:
     if counts is None:
         counts = expert_counts(spec)
     return 2 * min(int(counts.sum()), spec.M) * spec.N * spec.K
+
+
+@dataclasses.dataclass
+class RouteSpec:
+    """Inputs of the routing step: tokens before routing and a top-k choice of experts."""
+
+    name: str
+    batch: int
+    topk: int
+    K: int
+    E: int
+    x_dtype: int = E4M3
+    invalid: int = 0  # number of (token, k) slots given an expert id outside [0, E)
+    seed: int = 0
+
+    @property
+    def M(self) -> int:
+        return self.batch * self.topk
+
+    @property
+    def Ks(self) -> int:
+        return (self.K + 63) // 64
+
+
+def make_route_inputs(spec: RouteSpec) -> Dict[str, torch.Tensor]:
+    """topk_ids [batch, topk] int64 (distinct experts per token, uniformly random),
+    topk_weights [batch, topk] float32 (softmax of normals), x [batch, K] FP8 bytes,
+    x_scale [batch, ceil(K/64), 2] E8M0 bytes in 124..130."""
+    g = _gen("cpu", spec.seed)
+    scores = torch.rand((spec.batch, spec.E), generator=g)
+    ids = torch.topk(scores, k=min(spec.topk, spec.E), dim=1).indices.to(torch.int64)
+    if spec.topk > spec.E:
+        ids = torch.cat([ids, ids[:, : spec.topk - spec.E]], dim=1)
+    if spec.invalid:
+        flat = ids.view(-1)
+        pos = torch.randperm(flat.numel(), generator=g)[: spec.invalid]
+        flat[pos] = torch.where(torch.arange(spec.invalid) % 2 == 0, spec.E + 3, -1)
+    w = torch.softmax(torch.randn((spec.batch, spec.topk), generator=g), dim=1)
+    x = _fp8_bytes((spec.batch, spec.K), spec.x_dtype, g, "cpu")
+    xs = _e8m0_bytes((spec.batch, spec.Ks, 2), 124, 130, g, "cpu")
+    return dict(topk_ids=ids.contiguous(), topk_weights=w.contiguous(), x=x, x_scale=xs)
+
+
+def route_config(i: int) -> RouteSpec:
+    """Routing workloads with the batch / topk / K / E of benchmark workloads 1..5."""
+    s = config(i)
+    return RouteSpec(f"route {s.name.split()[0]} batch{s.batch} topk{s.M // s.batch} K{s.K} E{s.E}",
+                     batch=s.batch, topk=s.M // s.batch, K=s.K, E=s.E, x_dtype=s.x1_dtype, seed=2000 + i)
+
+
+def route_algorithmic_bytes(spec: RouteSpec) -> int:
+    """Reads: ids (8 B), weights (4 B), x and x_scale rows once; writes: x1, token
+    scales, row_index (8 B), logit (4 B), perm (4 B) per routed entry, group_list."""
+    M, K, Ks2 = spec.M, spec.K, 2 * spec.Ks
+    return M * 12 + spec.batch * (K + Ks2) + M * (K + Ks2 + 16) + spec.E * 8
