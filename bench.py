@@ -183,6 +183,42 @@ def _profiled_traffic(workload):
     return int(want["traffic-bytes-per-launch"]) if "traffic-bytes-per-launch" in want else None
 
 
+def _time_route(args, flush):
+    """Device time of the routing step (gmmfr_moe_route) for this workload's batch,
+    topk, K and E, with its own algorithmic bytes."""
+    import torch
+
+    from moe_grouped_gemm_mxfp8_gb300 import binding as B
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+    rs = W.route_config(args.config)
+    ri = {k: v.cuda() for k, v in W.make_route_inputs(rs).items()}
+    out, ws = B.route(ri["topk_ids"], ri["topk_weights"], ri["x"], ri["x_scale"], rs.E)
+    rp = B.RouteProblem(batch=rs.batch, topk=rs.topk, K=rs.K, E=rs.E, ids_type=B.INDEX_I64, group_list_type=1)
+    sptr = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        B.gmmfr_moe_route(rp, ri["topk_ids"].data_ptr(), ri["topk_weights"].data_ptr(), ri["x"].data_ptr(),
+                          ri["x_scale"].data_ptr(), out["x1"].data_ptr(), out["pertoken_scale"].data_ptr(),
+                          out["group_list"].data_ptr(), out["row_index"].data_ptr(), out["logit"].data_ptr(),
+                          out["perm"].data_ptr(), ws.data_ptr(), ws.numel(), sptr)
+
+    for _ in range(args.warmup):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        flush.zero_()
+        torch.cuda._sleep(200000)
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    nbytes = W.route_algorithmic_bytes(rs)
+    return {"workload": rs.name, "us_per_call": ms * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "algorithmic_bytes": nbytes, "launches": 3}
+
+
 def run_reference(args):
     """The oracle (CPU) as the reference arm: each step is a bounded column sample."""
     import torch
@@ -347,6 +383,7 @@ def run_ours(args):
         "clocks": clk.summary(),
         "wall_s_timed": t_wall,
     }
+    line["route"] = _time_route(args, flush)
     if rank == 0 and not args.no_cpu_baseline:
         cgbs, cdt, sample, cores = _cpu_baseline(spec, inp)
         line["cpu_baseline"] = {"value": cgbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}

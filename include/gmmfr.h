@@ -62,6 +62,7 @@ typedef enum { GMMFR_INDEX_I64 = 0, GMMFR_INDEX_I32 = 1 } gmmfr_index_type;
 #define GMMFR_DEV_BAD_GROUP_LIST 1u /* negative count, decreasing prefix sum, or total > M; ranges were clamped */
 #define GMMFR_DEV_BAD_ROW_INDEX 2u  /* a routed token had row_index outside [0, batch); it was skipped */
 #define GMMFR_DEV_TIMEOUT 4u        /* a pipeline wait gave up; the output is incomplete */
+#define GMMFR_DEV_BAD_EXPERT_ID 8u  /* routing: a top-k expert id outside [0, E); that entry was routed nowhere */
 
 /*
  * Sizes, formats and scalar arguments of one call (section 3.1 tensor table and
@@ -199,6 +200,48 @@ GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing_static_scratch(
     const gmmfr_problem* problem, const void* x1, const void* pertoken_scale, const int64_t* group_list,
     const float* logit, const void* row_index, const void* shared_input, float* out, const void* prepared,
     void* stream);
+
+/*
+ * The routing step before the operator (LLaDA2.0-mini grouped-GEMM write-up,
+ * section 5.2: argsort of the flattened expert ids, bincount, cumsum, and the
+ * tokens gathered in that order).  It produces the operator's x1,
+ * pertoken_scale, group_list, row_index and logit from tokens that are not yet
+ * routed and their top-k expert choice.
+ *
+ *   batch, topk   tokens and experts per token; M = batch * topk routed entries
+ *   K, E          row length of x (any K >= 1) and number of experts (1..1024)
+ *   ids_type      gmmfr_index_type of topk_ids
+ *   group_list_type  format of the produced group_list (0 prefix sums, 1 counts)
+ */
+typedef struct {
+  int64_t batch, topk, K, E;
+  int32_t ids_type;
+  int32_t group_list_type;
+} gmmfr_route_problem;
+
+/* Workspace bytes of gmmfr_moe_route (256-byte aligned).  Host only. */
+GMMFR_API gmmfr_status gmmfr_moe_route_workspace_size(const gmmfr_route_problem* problem, size_t* bytes);
+
+/*
+ * Entry f = b * topk + k (expert topk_ids[b, k]) goes to output position
+ *   (number of entries with a smaller expert id) + (entries of the same expert with a smaller f),
+ * i.e. a stable sort by expert; entries whose id lies outside [0, E) are placed
+ * after every routed entry (in ascending f), belong to no group, and set
+ * GMMFR_DEV_BAD_EXPERT_ID in the device error word of `workspace`.  At position p
+ * holding entry f:  x1[p] = x[f / topk], pertoken_scale[p] = x_scale[f / topk],
+ * row_index[p] = f / topk, logit[p] = topk_weights[f] (1 when topk_weights is NULL),
+ * perm[p] = f.
+ *   inputs   topk_ids [batch, topk]; topk_weights [batch, topk] float32 or NULL;
+ *            x [batch, K] FP8 bytes; x_scale [batch, ceil(K/64), 2] E8M0 bytes
+ *   outputs  x1 [M, K]; pertoken_scale [M, ceil(K/64), 2]; group_list [E] int64;
+ *            row_index [M] int64; logit [M] float32 or NULL; perm [M] int32 or NULL
+ * Three kernel launches; never syncs, never allocates.  Bit-exact and
+ * deterministic (byte and index work only).
+ */
+GMMFR_API gmmfr_status gmmfr_moe_route(const gmmfr_route_problem* problem, const void* topk_ids,
+                                       const float* topk_weights, const void* x, const void* x_scale, void* x1,
+                                       void* pertoken_scale, int64_t* group_list, int64_t* row_index, float* logit,
+                                       int32_t* perm, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Message of the last error returned on the calling thread ("" if none). */
 GMMFR_API const char* gmmfr_last_error(void);

@@ -29,7 +29,9 @@ ENTRY_POINTS = (
     "gmmfr_prepared_weights_size", "gmmfr_prepare_weights", "gmmfr_workspace_size",
     "gmmfr_grouped_matmul_finalize_routing", "gmmfr_check_device_errors", "gmmfr_last_error",
     "gmmfr_profile_begin", "gmmfr_profile_end", "gmmfr_grouped_matmul_finalize_routing_static_scratch",
+    "gmmfr_moe_route_workspace_size", "gmmfr_moe_route",
 )
+DEV_BAD_EXPERT_ID = 8
 
 
 class Problem(ctypes.Structure):
@@ -43,6 +45,14 @@ class Problem(ctypes.Structure):
         ("shared_rows", ctypes.c_int64), ("shared_offset", ctypes.c_int64),
         ("shared_weight", ctypes.c_float), ("flags", ctypes.c_uint32),
         ("expected_tokens_per_expert", ctypes.c_int64),
+    ]
+
+
+class RouteProblem(ctypes.Structure):
+    """Mirror of gmmfr_route_problem."""
+    _fields_ = [
+        ("batch", ctypes.c_int64), ("topk", ctypes.c_int64), ("K", ctypes.c_int64), ("E", ctypes.c_int64),
+        ("ids_type", ctypes.c_int32), ("group_list_type", ctypes.c_int32),
     ]
 
 
@@ -71,6 +81,9 @@ def load(path: str = LIB_PATH):
             lib.gmmfr_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
             lib.gmmfr_grouped_matmul_finalize_routing.argtypes = [P] + [vp] * 12 + [sz, vp]
             lib.gmmfr_grouped_matmul_finalize_routing_static_scratch.argtypes = [P] + [vp] * 9
+            RP = ctypes.POINTER(RouteProblem)
+            lib.gmmfr_moe_route_workspace_size.argtypes = [RP, ctypes.POINTER(sz)]
+            lib.gmmfr_moe_route.argtypes = [RP] + [vp] * 11 + [sz, vp]
             lib.gmmfr_check_device_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
             lib.gmmfr_last_error.restype = ctypes.c_char_p
             lib.gmmfr_profile_begin.argtypes = [ctypes.c_int]
@@ -149,6 +162,18 @@ def gmmfr_grouped_matmul_finalize_routing_static_scratch(problem: Problem, x1, p
         stream))
 
 
+def gmmfr_moe_route_workspace_size(problem: RouteProblem) -> int:
+    n = ctypes.c_size_t()
+    _check(load().gmmfr_moe_route_workspace_size(ctypes.byref(problem), ctypes.byref(n)))
+    return n.value
+
+
+def gmmfr_moe_route(problem: RouteProblem, topk_ids, topk_weights, x, x_scale, x1, pertoken_scale, group_list,
+                    row_index, logit, perm, workspace, workspace_bytes, stream=None) -> None:
+    _check(load().gmmfr_moe_route(ctypes.byref(problem), topk_ids, topk_weights, x, x_scale, x1, pertoken_scale,
+                                  group_list, row_index, logit, perm, workspace, workspace_bytes, stream))
+
+
 def gmmfr_check_device_errors(workspace: int, stream: Optional[int] = None) -> int:
     """Synchronises `stream`; returns the device error bits (0 when clean)."""
     bits = ctypes.c_uint32()
@@ -215,3 +240,27 @@ def run(problem: Problem, inputs: dict, out, prepared=None, ws=None, stream=None
         _ptr(inputs.get("shared_input")), _ptr(inputs.get("bias")), _ptr(out), _ptr(prepared), _ptr(ws),
         ws.numel(), _stream(stream))
     return ws
+
+
+def route(topk_ids, topk_weights, x, x_scale, E: int, group_list_type: int = 1, stream=None, ws=None):
+    """Run the routing step on device tensors; returns (dict of outputs, workspace)."""
+    import torch
+    batch, topk = topk_ids.shape
+    K = x.shape[1]
+    rp = RouteProblem(batch=batch, topk=topk, K=K, E=E,
+                      ids_type=INDEX_I32 if topk_ids.dtype == torch.int32 else INDEX_I64,
+                      group_list_type=group_list_type)
+    M = batch * topk
+    dev = x.device
+    o = dict(x1=torch.empty((M, K), dtype=torch.uint8, device=dev),
+             pertoken_scale=torch.empty((M,) + tuple(x_scale.shape[1:]), dtype=torch.uint8, device=dev),
+             group_list=torch.empty(E, dtype=torch.int64, device=dev),
+             row_index=torch.empty(M, dtype=torch.int64, device=dev),
+             logit=torch.empty(M, dtype=torch.float32, device=dev),
+             perm=torch.empty(M, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = torch.empty(max(gmmfr_moe_route_workspace_size(rp), 256), dtype=torch.uint8, device=dev)
+    gmmfr_moe_route(rp, _ptr(topk_ids), _ptr(topk_weights), _ptr(x), _ptr(x_scale), _ptr(o["x1"]),
+                    _ptr(o["pertoken_scale"]), _ptr(o["group_list"]), _ptr(o["row_index"]), _ptr(o["logit"]),
+                    _ptr(o["perm"]), _ptr(ws), ws.numel(), _stream(stream))
+    return o, ws

@@ -282,7 +282,7 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   int32_t* row_ptr = det ? reinterpret_cast<int32_t*>(ws + L.off_rowptr) : nullptr;
   int32_t* sorted = det ? reinterpret_cast<int32_t*>(ws + L.off_sorted) : nullptr;
   if (det) {
-    gmmfr::RouteParams rp{};
+    gmmfr::CsrParams rp{};
     rp.group_list = group_list;
     rp.row_index = row_index;
     rp.cnt = reinterpret_cast<int32_t*>(ws + L.off_cnt);
@@ -295,7 +295,7 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
     rp.group_list_type = p.group_list_type;
     rp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;
     timer.begin(1, s);
-    e = gmmfr::launch_route(rp, s);
+    e = gmmfr::launch_row_csr(rp, s);
     timer.end(1, s);
     if (e != cudaSuccess) return cuda_fail(e, "routing launch");
   }
@@ -363,6 +363,77 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
   timer.end(4, s);
+  return GMMFR_OK;
+}
+
+static gmmfr_status validate_route(const gmmfr_route_problem* p) {
+  if (!p) return fail(GMMFR_ERR_INVALID_ARG, "problem is NULL");
+  if (p->batch < 0 || p->topk < 1 || p->K < 1 || p->E < 1 || p->E > kMaxExperts)
+    return fail(GMMFR_ERR_INVALID_ARG, "batch=%lld topk=%lld K=%lld E=%lld out of range (batch >= 0, topk >= 1, K >= 1, 1 <= E <= 1024)",
+                (long long)p->batch, (long long)p->topk, (long long)p->K, (long long)p->E);
+  if (p->batch * p->topk >= (int64_t(1) << 31)) return fail(GMMFR_ERR_INVALID_ARG, "batch * topk must be below 2^31");
+  if (p->K >= (int64_t(1) << 31)) return fail(GMMFR_ERR_INVALID_ARG, "K must be below 2^31");
+  if (p->ids_type != GMMFR_INDEX_I64 && p->ids_type != GMMFR_INDEX_I32) return fail(GMMFR_ERR_INVALID_ARG, "ids_type=%d is not 0 or 1", p->ids_type);
+  if (p->group_list_type != 0 && p->group_list_type != 1) return fail(GMMFR_ERR_INVALID_ARG, "group_list_type=%d is not 0 or 1", p->group_list_type);
+  return GMMFR_OK;
+}
+
+static size_t route_ws_bytes(const gmmfr_route_problem* p) {
+  const int64_t M = p->batch * p->topk;
+  const int64_t tiles = cdiv(M, 256);
+  return gmmfr::kHdrBytes + align256(sizeof(int32_t) * (size_t)M) + align256(sizeof(int32_t) * (size_t)tiles * (p->E + 1));
+}
+
+gmmfr_status gmmfr_moe_route_workspace_size(const gmmfr_route_problem* problem, size_t* bytes) {
+  if (gmmfr_status st = validate_route(problem)) return st;
+  if (!bytes) return fail(GMMFR_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = route_ws_bytes(problem);
+  return GMMFR_OK;
+}
+
+gmmfr_status gmmfr_moe_route(const gmmfr_route_problem* problem, const void* topk_ids, const float* topk_weights,
+                             const void* x, const void* x_scale, void* x1, void* pertoken_scale, int64_t* group_list,
+                             int64_t* row_index, float* logit, int32_t* perm, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (gmmfr_status st = validate_route(problem)) return st;
+  const gmmfr_route_problem& p = *problem;
+  const int64_t M = p.batch * p.topk;
+  if (!group_list) return fail(GMMFR_ERR_INVALID_ARG, "group_list is NULL");
+  if (M > 0 && (!topk_ids || !x || !x_scale || !x1 || !pertoken_scale || !row_index))
+    return fail(GMMFR_ERR_INVALID_ARG, "topk_ids, x, x_scale, x1, pertoken_scale and row_index must be non-NULL when batch > 0");
+  if (!aligned(group_list, 8) || (row_index && !aligned(row_index, 8)) || (logit && !aligned(logit, 4)) ||
+      (perm && !aligned(perm, 4)) || (topk_weights && !aligned(topk_weights, 4)) ||
+      (topk_ids && !aligned(topk_ids, p.ids_type == GMMFR_INDEX_I32 ? 4 : 8)))
+    return fail(GMMFR_ERR_INVALID_ARG, "an input or output is not aligned to its element size");
+  const size_t need = route_ws_bytes(problem);
+  if (!workspace) return fail(GMMFR_ERR_WORKSPACE, "workspace is NULL (needs %zu bytes)", need);
+  if (workspace_bytes < need) return fail(GMMFR_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  if (!aligned(workspace, 256)) return fail(GMMFR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  gmmfr::RouteScatterParams rp{};
+  rp.topk_ids = topk_ids;
+  rp.topk_weights = topk_weights;
+  rp.x = static_cast<const uint8_t*>(x);
+  rp.x_scale = static_cast<const uint8_t*>(x_scale);
+  rp.x1 = static_cast<uint8_t*>(x1);
+  rp.pertoken_scale = static_cast<uint8_t*>(pertoken_scale);
+  rp.group_list = group_list;
+  rp.row_index = row_index;
+  rp.logit = logit;
+  rp.perm = perm;
+  rp.hdr = reinterpret_cast<uint32_t*>(ws);
+  rp.rank = reinterpret_cast<int32_t*>(ws + gmmfr::kHdrBytes);
+  rp.tile_counts = reinterpret_cast<int32_t*>(ws + gmmfr::kHdrBytes + align256(sizeof(int32_t) * (size_t)M));
+  rp.M = M;
+  rp.K = p.K;
+  rp.topk = p.topk;
+  rp.E = (int32_t)p.E;
+  rp.Ks = (int32_t)cdiv(p.K, 64);
+  rp.ids_i32 = p.ids_type == GMMFR_INDEX_I32;
+  rp.group_list_type = p.group_list_type;
+  rp.vec16 = (p.K % 16 == 0) && aligned(x, 16) && aligned(x1, 16);
+  cudaError_t e = gmmfr::launch_route_kernels(rp, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "routing launch");
   return GMMFR_OK;
 }
 

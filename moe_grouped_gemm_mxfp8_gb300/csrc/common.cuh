@@ -25,6 +25,7 @@ constexpr int kHdrBytes = 4096;
 constexpr uint32_t kErrBadGroupList = 1u;
 constexpr uint32_t kErrBadRowIndex = 2u;
 constexpr uint32_t kErrTimeout = 4u;
+constexpr uint32_t kErrBadExpertId = 8u;
 
 struct PrepParams {
   const uint8_t* x2;
@@ -37,7 +38,7 @@ struct PrepParams {
 };
 
 // Deterministic mode: tokens of each out row (CSR, unordered within a row).
-struct RouteParams {
+struct CsrParams {
   const int64_t* group_list;
   const void* row_index;
   int32_t* cnt;
@@ -87,9 +88,29 @@ struct CombineParams {
   int32_t split;
 };
 
+// MoE routing step (kernels_route.cu)
+struct RouteScatterParams {
+  const void* topk_ids;          // [M] int64 or int32
+  const float* topk_weights;     // [M] or null
+  const uint8_t* x;              // [batch, K]
+  const uint8_t* x_scale;        // [batch, 2*Ks]
+  uint8_t* x1;                   // [M, K]
+  uint8_t* pertoken_scale;       // [M, 2*Ks]
+  int64_t* group_list;           // [E]
+  int64_t* row_index;            // [M]
+  float* logit;                  // [M] or null
+  int32_t* perm;                 // [M] or null
+  int32_t* rank;                 // workspace [M]: stable rank of an entry within its tile and key
+  int32_t* tile_counts;          // workspace [tiles][E+1]: counts, then each tile's first position per key
+  uint32_t* hdr;                 // error words
+  int64_t M, K, topk;
+  int32_t E, Ks, ids_i32, group_list_type, vec16;
+};
+cudaError_t launch_route_kernels(const RouteScatterParams& p, cudaStream_t s);
+
 // launchers (defined next to their kernels)
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
-cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
+cudaError_t launch_row_csr(const CsrParams& p, cudaStream_t s);
 // x1 [M, K] as 2-D tensors of 128-byte rows, boxes of 16, 32, 64 and 128 rows (128-byte swizzle).
 struct TokenMaps {
   CUtensorMap m[4];

@@ -110,7 +110,7 @@ __device__ __forceinline__ int64_t load_row(const void* rows, int row_i32, int64
 // the GEMM kernel does: contiguous, clamped to [0, M]) to find the covered
 // tokens [0, covered), then builds the CSR of covered tokens by out row.
 // Positions within a row come from atomics; the combine kernel orders them.
-__global__ void __launch_bounds__(1024) route_kernel(RouteParams p) {
+__global__ void __launch_bounds__(1024) row_csr_kernel(CsrParams p) {
   __shared__ int64_t s_warp[32];
   __shared__ int64_t s_covered;
   const int tid = threadIdx.x;
@@ -155,8 +155,8 @@ __global__ void __launch_bounds__(1024) route_kernel(RouteParams p) {
   }
 }
 
-cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
-  route_kernel<<<1, 1024, 0, s>>>(p);
+cudaError_t launch_row_csr(const CsrParams& p, cudaStream_t s) {
+  row_csr_kernel<<<1, 1024, 0, s>>>(p);
   return cudaGetLastError();
 }
 

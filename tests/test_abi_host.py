@@ -140,3 +140,28 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(B, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         B.load(str(tmp_path / "missing.so"))
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(E=0), "out of range"), (dict(E=1025), "out of range"), (dict(topk=0), "out of range"),
+    (dict(batch=-1), "out of range"), (dict(K=0), "out of range"), (dict(ids_type=3), "ids_type"),
+    (dict(group_list_type=2), "group_list_type"),
+])
+def test_route_problem_validation(lib, kw, msg):
+    base = dict(batch=8, topk=2, K=128, E=4, ids_type=0, group_list_type=1)
+    base.update(kw)
+    rp = B.RouteProblem(**base)
+    with pytest.raises(B.GmmfrError, match=msg):
+        B.gmmfr_moe_route_workspace_size(rp)
+    with pytest.raises(B.GmmfrError):
+        B.gmmfr_moe_route(rp, None, None, None, None, None, None, None, None, None, None, None, 0)
+
+
+def test_route_rejects_missing_buffers(lib):
+    rp = B.RouteProblem(batch=8, topk=2, K=128, E=4, ids_type=0, group_list_type=1)
+    n = B.gmmfr_moe_route_workspace_size(rp)
+    assert n >= 4096 + 16 * 4
+    with pytest.raises(B.GmmfrError, match="must be non-NULL"):
+        B.gmmfr_moe_route(rp, None, None, None, None, None, None, 256, None, None, None, 256, n)
+    with pytest.raises(B.GmmfrError, match="workspace has"):
+        B.gmmfr_moe_route(rp, 256, None, 256, 256, 256, 256, 256, 256, None, None, 256, 16)
