@@ -302,3 +302,61 @@ def route_algorithmic_bytes(spec: RouteSpec) -> int:
     scales, row_index (8 B), logit (4 B), perm (4 B) per routed entry, group_list."""
     M, K, Ks2 = spec.M, spec.K, 2 * spec.Ks
     return M * 12 + spec.batch * (K + Ks2) + M * (K + Ks2 + 16) + spec.E * 8
+
+
+@dataclasses.dataclass
+class FfnSpec:
+    """Grouped SwiGLU expert FFN (BF16): sorted tokens, stacked gate|up and down weights."""
+
+    name: str
+    H: int
+    I: int
+    E: int
+    counts: tuple  # tokens per expert
+    scale: float = 0.02  # inputs and weights are randn * scale (the write-up's test uses 0.02)
+    seed: int = 42
+
+
+def make_ffn_inputs(spec: FfnSpec, device: str = "cpu", weights_device: Optional[str] = None) -> Dict[str, torch.Tensor]:
+    """sorted_tokens [N, H], w13_flat [E*H, 2I], w2_flat [E*I, H] (bf16), expert_cumsum [E+1] int32."""
+    weights_device = weights_device or device
+    g = _gen("cpu", spec.seed)
+    counts = torch.tensor(spec.counts, dtype=torch.int64)
+    assert counts.numel() == spec.E
+    N = int(counts.sum())
+    cs = torch.zeros(spec.E + 1, dtype=torch.int32)
+    cs[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    x = (torch.randn((N, spec.H), generator=g) * spec.scale).to(torch.bfloat16)
+    gw = _gen(weights_device, spec.seed + 7)
+    w13 = (torch.randn((spec.E * spec.H, 2 * spec.I), generator=gw, device=weights_device) * spec.scale).to(torch.bfloat16)
+    w2 = (torch.randn((spec.E * spec.I, spec.H), generator=gw, device=weights_device) * spec.scale).to(torch.bfloat16)
+    d = dict(sorted_tokens=x, w13_flat=w13, w2_flat=w2, expert_cumsum=cs)
+    if device != "cpu":
+        d = {k: v.to(device) for k, v in d.items()}
+    return d
+
+
+def ffn_config(name: str) -> FfnSpec:
+    """'test': the write-up's operator test (H 2048, I 512, counts 0,1,2,4,8,16,32,0);
+    'model': LLaDA2.0-mini shape (H 2048, I 512, E 256) with 4096 routed tokens spread
+    multinomially over the experts."""
+    if name == "test":
+        return FfnSpec("ffn test H2048 I512 E8", H=2048, I=512, E=8, counts=(0, 1, 2, 4, 8, 16, 32, 0))
+    if name == "model":
+        g = _gen("cpu", 4242)
+        draws = torch.multinomial(torch.full((256,), 1.0 / 256), 4096, replacement=True, generator=g)
+        c = tuple(torch.bincount(draws, minlength=256).tolist())
+        return FfnSpec("ffn model H2048 I512 E256 T4096", H=2048, I=512, E=256, counts=c)
+    raise ValueError(name)
+
+
+def ffn_algorithmic_bytes(spec: FfnSpec) -> int:
+    """w13 and w2 of experts holding tokens, tokens read, result written (all bf16)."""
+    nnz = sum(1 for c in spec.counts if c > 0)
+    N = sum(spec.counts)
+    return 2 * (nnz * spec.H * 2 * spec.I + nnz * spec.I * spec.H + 2 * N * spec.H) + 4 * (spec.E + 1)
+
+
+def ffn_flops(spec: FfnSpec) -> int:
+    N = sum(spec.counts)
+    return 2 * N * spec.H * 2 * spec.I + 2 * N * spec.I * spec.H
