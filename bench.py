@@ -219,6 +219,35 @@ def _time_route(args, flush):
             "algorithmic_bytes": nbytes, "launches": 3}
 
 
+def _time_ffn(args, flush):
+    """Device time of the grouped SwiGLU FFN (gmmfr_llada2_moe_grouped_gemm) on the
+    LLaDA2.0-mini shape (H 2048, I 512, E 256, 4096 routed tokens)."""
+    import torch
+
+    from moe_grouped_gemm_mxfp8_gb300 import binding as B
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+    fs = W.ffn_config("model")
+    d = {k: v.cuda() for k, v in W.make_ffn_inputs(fs, weights_device="cuda").items()}
+    prep = B.ffn_prepare(fs.H, fs.I, fs.E, d["w13_flat"], d["w2_flat"])
+    res, ws = B.ffn(d["sorted_tokens"], prep, d["expert_cumsum"], fs.H, fs.I, fs.E)
+    for _ in range(args.warmup):
+        B.ffn(d["sorted_tokens"], prep, d["expert_cumsum"], fs.H, fs.I, fs.E, result=res, ws=ws)
+    B.gmmfr_profile_begin(args.steps)
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda._sleep(200000)
+        B.ffn(d["sorted_tokens"], prep, d["expert_cumsum"], fs.H, fs.I, fs.E, result=res, ws=ws)
+    k = B.gmmfr_profile_end(args.steps)
+    ms = statistics.mean(x[4] for x in k)
+    nbytes = W.ffn_algorithmic_bytes(fs)
+    peaks, _ = _peaks()
+    return {"workload": fs.name, "us_per_call": ms * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+            "gemm1_us": statistics.mean(x[2] for x in k) * 1e3, "gemm2_us": statistics.mean(x[3] for x in k) * 1e3,
+            "tflops": W.ffn_flops(fs) / (ms * 1e-3) / 1e12, "algorithmic_bytes": nbytes, "launches": 2}
+
+
 def run_reference(args):
     """The oracle (CPU) as the reference arm: each step is a bounded column sample."""
     import torch
@@ -384,6 +413,7 @@ def run_ours(args):
         "wall_s_timed": t_wall,
     }
     line["route"] = _time_route(args, flush)
+    line["ffn"] = _time_ffn(args, flush)
     if rank == 0 and not args.no_cpu_baseline:
         cgbs, cdt, sample, cores = _cpu_baseline(spec, inp)
         line["cpu_baseline"] = {"value": cgbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}

@@ -243,6 +243,43 @@ GMMFR_API gmmfr_status gmmfr_moe_route(const gmmfr_route_problem* problem, const
                                        void* pertoken_scale, int64_t* group_list, int64_t* row_index, float* logit,
                                        int32_t* perm, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Grouped SwiGLU expert FFN in BF16 (llada2_moe_grouped_gemm; LLaDA2.0-mini
+ * grouped-GEMM write-up, sections 3.1-3.3).  For every expert e and its sorted
+ * token rows [expert_cumsum[e], expert_cumsum[e+1]):
+ *   gate_up = x @ w13_flat[e*H:(e+1)*H, :]   (FP32 accumulate; gate = first I columns, up = last I)
+ *   sw      = bf16(SiLU(gate) * up),  SiLU(g) = g / (1 + exp(-g))
+ *   result  = bf16(sw @ w2_flat[e*I:(e+1)*I, :])
+ * Rows outside every expert range are left untouched.
+ *   N  rows of sorted_tokens and result;  H, I  hidden and intermediate sizes
+ *      (multiples of 8);  E  experts (1..1024)
+ */
+typedef struct {
+  int64_t N, H, I, E;
+} gmmfr_ffn_problem;
+
+/* Bytes of the prepared FFN weights (E*ceil(I/64)*ceil(H/64) + E*ceil(H/128)*ceil(I/64) tiles of 16 KB). */
+GMMFR_API gmmfr_status gmmfr_ffn_prepared_weights_size(const gmmfr_ffn_problem* problem, size_t* bytes);
+
+/* One-time re-layout of w13_flat [E*H, 2I] and w2_flat [E*I, H] (bf16) into swizzled
+ * 128-row tiles (a w13 tile holds 64 gate columns and the 64 up columns of the same
+ * indices); `prepared` is a caller buffer, 16-byte aligned, fully overwritten. */
+GMMFR_API gmmfr_status gmmfr_ffn_prepare_weights(const gmmfr_ffn_problem* problem, const void* w13_flat,
+                                                 const void* w2_flat, void* prepared, size_t prepared_bytes,
+                                                 void* stream);
+
+/* Workspace bytes of gmmfr_llada2_moe_grouped_gemm (error words + the bf16 sw rows). */
+GMMFR_API gmmfr_status gmmfr_ffn_workspace_size(const gmmfr_ffn_problem* problem, size_t* bytes);
+
+/* The grouped FFN: sorted_tokens [N, H] bf16, expert_cumsum [E+1] int32 (checked on the
+ * device: non-decreasing, within [0, N]; violations set GMMFR_DEV_BAD_GROUP_LIST and are
+ * clamped), result [N, H] bf16.  Two kernel launches; no sync, no allocation; every
+ * result element is written by one thread (deterministic). */
+GMMFR_API gmmfr_status gmmfr_llada2_moe_grouped_gemm(const gmmfr_ffn_problem* problem, const void* sorted_tokens,
+                                                     const void* prepared, const int32_t* expert_cumsum,
+                                                     void* result, void* workspace, size_t workspace_bytes,
+                                                     void* stream);
+
 /* Message of the last error returned on the calling thread ("" if none). */
 GMMFR_API const char* gmmfr_last_error(void);
 

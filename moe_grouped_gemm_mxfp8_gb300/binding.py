@@ -30,6 +30,8 @@ ENTRY_POINTS = (
     "gmmfr_grouped_matmul_finalize_routing", "gmmfr_check_device_errors", "gmmfr_last_error",
     "gmmfr_profile_begin", "gmmfr_profile_end", "gmmfr_grouped_matmul_finalize_routing_static_scratch",
     "gmmfr_moe_route_workspace_size", "gmmfr_moe_route",
+    "gmmfr_ffn_prepared_weights_size", "gmmfr_ffn_prepare_weights", "gmmfr_ffn_workspace_size",
+    "gmmfr_llada2_moe_grouped_gemm",
 )
 DEV_BAD_EXPERT_ID = 8
 
@@ -54,6 +56,11 @@ class RouteProblem(ctypes.Structure):
         ("batch", ctypes.c_int64), ("topk", ctypes.c_int64), ("K", ctypes.c_int64), ("E", ctypes.c_int64),
         ("ids_type", ctypes.c_int32), ("group_list_type", ctypes.c_int32),
     ]
+
+
+class FfnProblem(ctypes.Structure):
+    """Mirror of gmmfr_ffn_problem."""
+    _fields_ = [("N", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64), ("E", ctypes.c_int64)]
 
 
 class GmmfrError(RuntimeError):
@@ -84,6 +91,11 @@ def load(path: str = LIB_PATH):
             RP = ctypes.POINTER(RouteProblem)
             lib.gmmfr_moe_route_workspace_size.argtypes = [RP, ctypes.POINTER(sz)]
             lib.gmmfr_moe_route.argtypes = [RP] + [vp] * 11 + [sz, vp]
+            FP = ctypes.POINTER(FfnProblem)
+            lib.gmmfr_ffn_prepared_weights_size.argtypes = [FP, ctypes.POINTER(sz)]
+            lib.gmmfr_ffn_prepare_weights.argtypes = [FP, vp, vp, vp, sz, vp]
+            lib.gmmfr_ffn_workspace_size.argtypes = [FP, ctypes.POINTER(sz)]
+            lib.gmmfr_llada2_moe_grouped_gemm.argtypes = [FP, vp, vp, vp, vp, vp, sz, vp]
             lib.gmmfr_check_device_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
             lib.gmmfr_last_error.restype = ctypes.c_char_p
             lib.gmmfr_profile_begin.argtypes = [ctypes.c_int]
@@ -172,6 +184,28 @@ def gmmfr_moe_route(problem: RouteProblem, topk_ids, topk_weights, x, x_scale, x
                     row_index, logit, perm, workspace, workspace_bytes, stream=None) -> None:
     _check(load().gmmfr_moe_route(ctypes.byref(problem), topk_ids, topk_weights, x, x_scale, x1, pertoken_scale,
                                   group_list, row_index, logit, perm, workspace, workspace_bytes, stream))
+
+
+def gmmfr_ffn_prepared_weights_size(problem: FfnProblem) -> int:
+    n = ctypes.c_size_t()
+    _check(load().gmmfr_ffn_prepared_weights_size(ctypes.byref(problem), ctypes.byref(n)))
+    return n.value
+
+
+def gmmfr_ffn_prepare_weights(problem: FfnProblem, w13_flat, w2_flat, prepared, prepared_bytes, stream=None) -> None:
+    _check(load().gmmfr_ffn_prepare_weights(ctypes.byref(problem), w13_flat, w2_flat, prepared, prepared_bytes, stream))
+
+
+def gmmfr_ffn_workspace_size(problem: FfnProblem) -> int:
+    n = ctypes.c_size_t()
+    _check(load().gmmfr_ffn_workspace_size(ctypes.byref(problem), ctypes.byref(n)))
+    return n.value
+
+
+def gmmfr_llada2_moe_grouped_gemm(problem: FfnProblem, sorted_tokens, prepared, expert_cumsum, result, workspace,
+                                  workspace_bytes, stream=None) -> None:
+    _check(load().gmmfr_llada2_moe_grouped_gemm(ctypes.byref(problem), sorted_tokens, prepared, expert_cumsum,
+                                                result, workspace, workspace_bytes, stream))
 
 
 def gmmfr_check_device_errors(workspace: int, stream: Optional[int] = None) -> int:
@@ -264,3 +298,27 @@ def route(topk_ids, topk_weights, x, x_scale, E: int, group_list_type: int = 1, 
                     _ptr(o["pertoken_scale"]), _ptr(o["group_list"]), _ptr(o["row_index"]), _ptr(o["logit"]),
                     _ptr(o["perm"]), _ptr(ws), ws.numel(), _stream(stream))
     return o, ws
+
+
+def ffn_prepare(H: int, I: int, E: int, w13_flat, w2_flat, stream=None):
+    """Prepared-weight buffer (torch uint8) for the grouped FFN."""
+    import torch
+    fp = FfnProblem(N=0, H=H, I=I, E=E)
+    n = gmmfr_ffn_prepared_weights_size(fp)
+    buf = torch.empty(n, dtype=torch.uint8, device=w13_flat.device)
+    gmmfr_ffn_prepare_weights(fp, _ptr(w13_flat), _ptr(w2_flat), _ptr(buf), n, _stream(stream))
+    return buf
+
+
+def ffn(sorted_tokens, prepared, expert_cumsum, H: int, I: int, E: int, result=None, ws=None, stream=None):
+    """Run the grouped FFN on device tensors; returns (result, workspace)."""
+    import torch
+    N = sorted_tokens.shape[0]
+    fp = FfnProblem(N=N, H=H, I=I, E=E)
+    if result is None:
+        result = torch.zeros((N, H), dtype=torch.bfloat16, device=sorted_tokens.device)
+    if ws is None:
+        ws = torch.empty(gmmfr_ffn_workspace_size(fp), dtype=torch.uint8, device=sorted_tokens.device)
+    gmmfr_llada2_moe_grouped_gemm(fp, _ptr(sorted_tokens), _ptr(prepared), _ptr(expert_cumsum), _ptr(result),
+                                  _ptr(ws), ws.numel(), _stream(stream))
+    return result, ws

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgmmfr.so")
-SOURCES = ["api.cu", "kernels_aux.cu", "kernels_gemm.cu", "kernels_route.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "kernels_aux.cu", "kernels_ffn.cu", "kernels_gemm.cu", "kernels_route.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -437,6 +437,149 @@ gmmfr_status gmmfr_moe_route(const gmmfr_route_problem* problem, const void* top
   return GMMFR_OK;
 }
 
+static gmmfr_status validate_ffn(const gmmfr_ffn_problem* p) {
+  if (!p) return fail(GMMFR_ERR_INVALID_ARG, "problem is NULL");
+  if (p->N < 0 || p->N >= (int64_t(1) << 31) || p->H < 8 || p->I < 8 || p->H % 8 || p->I % 8 ||
+      p->H >= (int64_t(1) << 24) || p->I >= (int64_t(1) << 24) || p->E < 1 || p->E > kMaxExperts)
+    return fail(GMMFR_ERR_INVALID_ARG, "N=%lld H=%lld I=%lld E=%lld out of range (N >= 0; H, I multiples of 8; 1 <= E <= 1024)",
+                (long long)p->N, (long long)p->H, (long long)p->I, (long long)p->E);
+  return GMMFR_OK;
+}
+
+static void ffn_tiles(const gmmfr_ffn_problem* p, int64_t& nt1, int64_t& kb1, int64_t& nt2, int64_t& kb2) {
+  nt1 = cdiv(p->I, 64);
+  kb1 = cdiv(p->H, 64);
+  nt2 = cdiv(p->H, 128);
+  kb2 = cdiv(p->I, 64);
+}
+
+gmmfr_status gmmfr_ffn_prepared_weights_size(const gmmfr_ffn_problem* problem, size_t* bytes) {
+  if (gmmfr_status st = validate_ffn(problem)) return st;
+  if (!bytes) return fail(GMMFR_ERR_INVALID_ARG, "bytes is NULL");
+  int64_t nt1, kb1, nt2, kb2;
+  ffn_tiles(problem, nt1, kb1, nt2, kb2);
+  *bytes = (size_t)problem->E * (nt1 * kb1 + nt2 * kb2) * gmmfr::kWTileBytes;
+  return GMMFR_OK;
+}
+
+gmmfr_status gmmfr_ffn_prepare_weights(const gmmfr_ffn_problem* problem, const void* w13_flat, const void* w2_flat,
+                                       void* prepared, size_t prepared_bytes, void* stream) {
+  if (gmmfr_status st = validate_ffn(problem)) return st;
+  size_t need = 0;
+  gmmfr_ffn_prepared_weights_size(problem, &need);
+  if (!w13_flat || !w2_flat || !prepared) return fail(GMMFR_ERR_INVALID_ARG, "w13_flat, w2_flat and prepared must be non-NULL");
+  if (prepared_bytes < need) return fail(GMMFR_ERR_WORKSPACE, "prepared buffer has %zu bytes, needs %zu", prepared_bytes, need);
+  if (!aligned(prepared, 16) || !aligned(w13_flat, 2) || !aligned(w2_flat, 2))
+    return fail(GMMFR_ERR_INVALID_ARG, "prepared must be 16-byte aligned and the weights 2-byte aligned");
+  gmmfr::FfnPrepParams pp{};
+  int64_t nt1, kb1, nt2, kb2;
+  ffn_tiles(problem, nt1, kb1, nt2, kb2);
+  pp.w13 = static_cast<const uint16_t*>(w13_flat);
+  pp.w2 = static_cast<const uint16_t*>(w2_flat);
+  pp.prepared = static_cast<uint8_t*>(prepared);
+  pp.H = problem->H;
+  pp.I = problem->I;
+  pp.E = (int32_t)problem->E;
+  pp.NT1 = (int32_t)nt1;
+  pp.KB1 = (int32_t)kb1;
+  pp.NT2 = (int32_t)nt2;
+  pp.KB2 = (int32_t)kb2;
+  cudaError_t e = gmmfr::launch_ffn_prep(pp, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "FFN weight preparation launch");
+  return GMMFR_OK;
+}
+
+static size_t ffn_ws_bytes(const gmmfr_ffn_problem* p) {
+  return gmmfr::kHdrBytes + align256(sizeof(uint16_t) * (size_t)p->N * p->I);
+}
+
+gmmfr_status gmmfr_ffn_workspace_size(const gmmfr_ffn_problem* problem, size_t* bytes) {
+  if (gmmfr_status st = validate_ffn(problem)) return st;
+  if (!bytes) return fail(GMMFR_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = ffn_ws_bytes(problem);
+  return GMMFR_OK;
+}
+
+// 2-D bf16 tensor [rows, cols] with 128-byte (64-element) boxes of 16/32/64/128 rows
+static gmmfr_status encode_bf16_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* base, int64_t rows,
+                                     int64_t cols, void* dummy, gmmfr::TokenMaps& maps) {
+  const bool empty = rows == 0;
+  cuuint64_t dims[2] = {(cuuint64_t)(empty ? 8 : cols), (cuuint64_t)(empty ? 1 : rows)};
+  cuuint64_t strides[1] = {(cuuint64_t)(empty ? 16 : cols * 2)};
+  cuuint32_t estr[2] = {1, 1};
+  for (int b = 0; b < 4; ++b) {
+    cuuint32_t box[2] = {64, (cuuint32_t)(gmmfr::kTokBox << b)};
+    CUresult r = encode(&maps.m[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, empty ? dummy : const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GMMFR_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  }
+  return GMMFR_OK;
+}
+
+gmmfr_status gmmfr_llada2_moe_grouped_gemm(const gmmfr_ffn_problem* problem, const void* sorted_tokens,
+                                           const void* prepared, const int32_t* expert_cumsum, void* result,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (gmmfr_status st = validate_ffn(problem)) return st;
+  const gmmfr_ffn_problem& p = *problem;
+  if (!expert_cumsum || !prepared) return fail(GMMFR_ERR_INVALID_ARG, "expert_cumsum and prepared must be non-NULL");
+  if (p.N > 0 && (!sorted_tokens || !result)) return fail(GMMFR_ERR_INVALID_ARG, "sorted_tokens and result must be non-NULL when N > 0");
+  if (!aligned(prepared, 16) || !aligned(expert_cumsum, 4) || (sorted_tokens && !aligned(sorted_tokens, 16)) ||
+      (result && !aligned(result, 2)))
+    return fail(GMMFR_ERR_INVALID_ARG, "sorted_tokens and prepared must be 16-byte aligned, result 2-byte, expert_cumsum 4-byte");
+  const size_t need = ffn_ws_bytes(problem);
+  if (!workspace) return fail(GMMFR_ERR_WORKSPACE, "workspace is NULL (needs %zu bytes)", need);
+  if (workspace_bytes < need) return fail(GMMFR_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  if (!aligned(workspace, 256)) return fail(GMMFR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+  if (!encode) return fail(GMMFR_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* sw = ws + gmmfr::kHdrBytes;
+  gmmfr::TokenMaps m1, m2;
+  if (gmmfr_status st = encode_bf16_maps(encode, sorted_tokens, p.N, p.H, ws, m1)) return st;
+  if (gmmfr_status st = encode_bf16_maps(encode, sw, p.N, p.I, ws, m2)) return st;
+  int64_t nt1, kb1, nt2, kb2;
+  ffn_tiles(problem, nt1, kb1, nt2, kb2);
+  const int grid = std::min(device_sms(), gmmfr::kMaxErrSlots / 2);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  gmmfr::FfnParams fp{};
+  fp.cumsum = expert_cumsum;
+  fp.hdr = reinterpret_cast<uint32_t*>(ws);
+  fp.N = p.N;
+  fp.E = (int32_t)p.E;
+  // kind::f16: FP32 accumulator (bits 4..5 = 1), A and B BF16 (bits 7..9, 10..12 = 1), M = 128
+  fp.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 4) << 24);
+  fp.timeout_ns = 4000000000ll;
+  // GEMM1: tokens x w13 -> sw (SwiGLU in the epilogue)
+  fp.prepared = static_cast<const uint8_t*>(prepared);
+  fp.out = static_cast<__nv_bfloat16*>(sw);
+  fp.out_cols = p.I;
+  fp.NT = (int32_t)nt1;
+  fp.KB = (int32_t)kb1;
+  fp.gate_up = 1;
+  fp.slot_base = 0;
+  CallTimer timer;
+  timer.begin(4, s);
+  timer.begin(2, s);
+  cudaError_t e = gmmfr::launch_ffn_gemm(m1, fp, grid, s);
+  timer.end(2, s);
+  if (e != cudaSuccess) return cuda_fail(e, "FFN gate/up GEMM launch");
+  // GEMM2: sw x w2 -> result
+  fp.prepared = static_cast<const uint8_t*>(prepared) + (size_t)p.E * nt1 * kb1 * gmmfr::kWTileBytes;
+  fp.out = static_cast<__nv_bfloat16*>(result);
+  fp.out_cols = p.H;
+  fp.NT = (int32_t)nt2;
+  fp.KB = (int32_t)kb2;
+  fp.gate_up = 0;
+  fp.slot_base = grid;
+  timer.begin(3, s);
+  e = gmmfr::launch_ffn_gemm(m2, fp, grid, s);
+  timer.end(3, s);
+  timer.end(4, s);
+  if (e != cudaSuccess) return cuda_fail(e, "FFN down GEMM launch");
+  return GMMFR_OK;
+}
+
 gmmfr_status gmmfr_check_device_errors(const void* workspace, void* stream, uint32_t* bits) {
   if (!workspace || !bits) return fail(GMMFR_ERR_INVALID_ARG, "workspace and bits must be non-NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -1,6 +1,7 @@
 // Internal definitions shared by the host API and the kernels of the library.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -107,6 +108,31 @@ struct RouteScatterParams {
   int32_t E, Ks, ids_i32, group_list_type, vec16;
 };
 cudaError_t launch_route_kernels(const RouteScatterParams& p, cudaStream_t s);
+
+// Grouped SwiGLU expert FFN (kernels_ffn.cu)
+struct FfnPrepParams {
+  const uint16_t* w13;  // [E*H, 2I] bf16
+  const uint16_t* w2;   // [E*I, H] bf16
+  uint8_t* prepared;
+  int64_t H, I;
+  int32_t E, NT1, KB1, NT2, KB2;
+};
+struct FfnParams {
+  const uint8_t* prepared;  // tiles of this GEMM
+  const int32_t* cumsum;    // [E+1]
+  __nv_bfloat16* out;       // GEMM1: sw [N, I]; GEMM2: result [N, H]
+  uint32_t* hdr;
+  int64_t N;
+  int64_t out_cols;         // I (GEMM1) or H (GEMM2)
+  int32_t E, NT, KB;
+  int32_t gate_up;          // 1: SwiGLU epilogue
+  int32_t slot_base;        // first error slot of this launch
+  uint32_t idesc;
+  int64_t timeout_ns;
+};
+struct TokenMaps;
+cudaError_t launch_ffn_prep(const FfnPrepParams& p, cudaStream_t s);
+cudaError_t launch_ffn_gemm(const TokenMaps& tmaps, const FfnParams& p, int grid, cudaStream_t s);
 
 // launchers (defined next to their kernels)
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);

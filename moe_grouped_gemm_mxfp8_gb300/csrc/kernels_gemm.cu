@@ -34,6 +34,7 @@
 // Every wait is bounded: on timeout the CTA sets GMMFR_DEV_TIMEOUT, stops
 // issuing, waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
 #include "common.cuh"
+#include "pipeline.cuh"
 #include "ptx.cuh"
 
 namespace gmmfr {
@@ -142,77 +143,12 @@ struct Groups {
   }
 };
 
-struct Ctl {
-  volatile int* abort;
-  uint32_t* err;  // shared-memory error bits of this CTA
-  int64_t timeout_ns;
-};
-
-// Bounded wait for the phase of `parity` to complete.  Gives up when another
-// role aborted or after timeout_ns (then records the timeout and aborts).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*c.abort) return false;
-    if (ptx::globaltimer() - t0 > (uint64_t)c.timeout_ns) {
-      *c.abort = 1;
-      atomicOr(c.err, kErrTimeout);
-      return false;
-    }
-  }
-}
-
-// wait_bar for a whole warp: every lane waits in hardware (the warp stays
-// converged and sleeps in try_wait), then a vote makes the outcome uniform, so
-// a timeout seen by one lane can never split the warp.
-__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
-  const bool ok = wait_bar(bar, parity, c);
-  return __all_sync(0xffffffffu, ok) != 0;
-}
-
-// Wait used while draining after an abort: ignores the abort flag, fixed 1 s limit.
-__device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer() - t0 > 1000000000ull) return false;
-  }
-  return true;
-}
-
 __device__ __forceinline__ int load_row32(const void* rows, int row_i32, int64_t t, int64_t batch) {
   const int64_t r = row_i32 ? (int64_t) static_cast<const int32_t*>(rows)[t] : static_cast<const int64_t*>(rows)[t];
   return (r >= 0 && r < batch) ? (int)r : -1;
 }
 
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-
-// Block-wide inclusive scan (sum or max) over the kGemmThreads threads; `total`
-// gets the last value.  Every thread must call it.
-template <bool kMax>
-__device__ int64_t cta_scan(int64_t v, int64_t* scratch, int64_t& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kWarps = kGemmThreads / 32;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v = kMax ? (u > v ? u : v) : v + u;
-  }
-  if (lane == 31) scratch[warp] = v;
-  __syncthreads();
-  int64_t carry = kMax ? INT64_MIN : 0, all = kMax ? INT64_MIN : 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const int64_t u = scratch[w];
-    if (w < warp) carry = kMax ? (u > carry ? u : carry) : carry + u;
-    all = kMax ? (u > all ? u : all) : all + u;
-  }
-  if (warp > 0) v = kMax ? (carry > v ? carry : v) : v + carry;
-  total = all;
-  __syncthreads();
-  return v;
-}
 
 // Expert ranges (MXFP8 grouped_matmul_finalize_routing write-up, section 4.3:
 // type 0 prefix sums, type 1 counts),
@@ -231,13 +167,13 @@ __device__ int decode_groups(const GemmParams& p, int32_t* s_end, int32_t* s_gba
     if (p.group_list_type == 1) {
       if (e < E && g < 0) atomicOr(s_err, kErrBadGroupList);
       const int64_t c = e < E ? (g < 0 ? 0 : (g > M ? M + 1 : g)) : 0;
-      v = cta_scan<false>(c, scratch, tot) + carry;
+      v = cta_scan<false, kGemmThreads>(c, scratch, tot) + carry;
       carry += tot;
     } else {
       const int64_t prev = (e > 0 && e < E) ? p.group_list[e - 1] : 0;
       if (e < E && (g < prev || g > M)) atomicOr(s_err, kErrBadGroupList);
       const int64_t c = e < E ? (g < 0 ? 0 : (g > M ? M : g)) : 0;
-      v = cta_scan<true>(c, scratch, tot);
+      v = cta_scan<true, kGemmThreads>(c, scratch, tot);
       v = v > carry ? v : carry;
       carry = tot > carry ? tot : carry;
     }
@@ -252,7 +188,7 @@ __device__ int decode_groups(const GemmParams& p, int32_t* s_end, int32_t* s_gba
     mx = c > mx ? c : mx;
   }
   int64_t mx_all;
-  cta_scan<true>(mx, scratch, mx_all);
+  cta_scan<true, kGemmThreads>(mx, scratch, mx_all);
   int tmax = mx_all <= 32 ? 32 : (mx_all <= 64 ? 64 : 128);
   if (p.tmax_fixed) tmax = p.tmax_fixed;
   // first group of every expert
@@ -262,7 +198,7 @@ __device__ int decode_groups(const GemmParams& p, int32_t* s_end, int32_t* s_gba
     const int64_t c = e < E ? s_end[e] - (e ? s_end[e - 1] : 0) : 0;
     const int64_t ng = (c + tmax - 1) / tmax;
     int64_t tot;
-    const int64_t incl = cta_scan<false>(ng, scratch, tot) + gcarry;
+    const int64_t incl = cta_scan<false, kGemmThreads>(ng, scratch, tot) + gcarry;
     if (e < E) s_gbase[e] = (int32_t)(incl - ng);
     gcarry += tot;
   }

@@ -165,3 +165,20 @@ def test_route_rejects_missing_buffers(lib):
         B.gmmfr_moe_route(rp, None, None, None, None, None, None, 256, None, None, None, 256, n)
     with pytest.raises(B.GmmfrError, match="workspace has"):
         B.gmmfr_moe_route(rp, 256, None, 256, 256, 256, 256, 256, 256, None, None, 256, 16)
+
+
+@pytest.mark.parametrize("kw", [dict(H=100), dict(I=4), dict(E=0), dict(N=-1), dict(E=2000)])
+def test_ffn_problem_validation(lib, kw):
+    base = dict(N=16, H=128, I=64, E=4)
+    base.update(kw)
+    fp = B.FfnProblem(**base)
+    with pytest.raises(B.GmmfrError, match="out of range"):
+        B.gmmfr_ffn_workspace_size(fp)
+    with pytest.raises(B.GmmfrError):
+        B.gmmfr_llada2_moe_grouped_gemm(fp, None, None, None, None, None, 0)
+
+
+def test_ffn_sizes(lib):
+    fp = B.FfnProblem(N=4096, H=2048, I=512, E=256)
+    assert B.gmmfr_ffn_prepared_weights_size(fp) == 256 * (8 * 32 + 16 * 8) * 16384
+    assert B.gmmfr_ffn_workspace_size(fp) == 4096 + 4096 * 512 * 2
