@@ -27,6 +27,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "µs/call and achieved HBM GB/s vs roofline, MXFP8 grouped-matmul-finalize-routing"
 DEFAULT_CONFIG = 2
+FMT_NAMES = {0: "E4M3", 1: "E5M2", 2: "E2M1"}
 
 
 def reduce_step_time(ms: float, world: int) -> float:
@@ -57,7 +58,7 @@ def _peaks():
 
 def _config_dict(spec, counts, deterministic):
     return {"workload": spec.name, "M": spec.M, "K": spec.K, "N": spec.N, "E": spec.E, "batch": spec.batch,
-            "x1": "E5M2" if spec.x1_dtype else "E4M3", "x2": "E5M2" if spec.x2_dtype else "E4M3",
+            "x1": FMT_NAMES[spec.x1_dtype], "x2": FMT_NAMES[spec.x2_dtype],
             "transpose_x2": spec.transpose_x2, "group_list_type": spec.group_list_type,
             "nonempty_experts": int((counts > 0).sum()), "max_tokens_per_expert": int(counts.max()),
             "mode": "deterministic" if deterministic else "atomic",
@@ -248,6 +249,44 @@ def _time_ffn(args, flush):
             "tflops": W.ffn_flops(fs) / (ms * 1e-3) / 1e12, "algorithmic_bytes": nbytes, "launches": 2}
 
 
+def _time_mxfp4(args, flush):
+    """Device time of the operator on MXFP4 inputs (E2M1 tokens and weights, E8M0 per
+    32) at the large shape (M 4096, K 7168, N 4096, E 256), against the algorithmic
+    bytes of the packed FP4 inputs.  The prepared weights are E4M3 tiles, so a call
+    reads twice the FP4 weight bytes."""
+    import torch
+
+    from moe_grouped_gemm_mxfp8_gb300 import binding as B
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+    spec = W.mxfp4_config()
+    inp = W.make_inputs(spec, weights_device="cuda")
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    prob = B.problem_from_spec(spec)
+    prep = B.prepare_weights(prob, d["x2"], d["scale"])
+    del d["x2"]
+    ws = B.workspace(prob, True, "cuda")
+    out = d["out"].clone()
+    for _ in range(args.warmup):
+        B.run(prob, d, out, prepared=prep, ws=ws)
+    B.gmmfr_profile_begin(args.steps)
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda._sleep(200000)
+        B.run(prob, d, out, prepared=prep, ws=ws)
+    k = B.gmmfr_profile_end(args.steps)
+    bits = B.gmmfr_check_device_errors(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    ms = statistics.mean(x[4] for x in k)
+    nbytes = W.algorithmic_bytes(spec)
+    peaks, _ = _peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del prep, ws
+    return {"workload": spec.name, "us_per_call": ms * 1e3, "gbs": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"]),
+            "expand_us": statistics.mean(x[0] for x in k) * 1e3, "gemm_us": statistics.mean(x[2] for x in k) * 1e3,
+            "tflops": W.flops(spec) / (ms * 1e-3) / 1e12, "algorithmic_bytes": nbytes, "launches": 2,
+            "device_error_bits": bits}
+
+
 def run_reference(args):
     """The oracle (CPU) as the reference arm: each step is a bounded column sample."""
     import torch
@@ -414,6 +453,7 @@ def run_ours(args):
     }
     line["route"] = _time_route(args, flush)
     line["ffn"] = _time_ffn(args, flush)
+    line["mxfp4"] = _time_mxfp4(args, flush)
     if rank == 0 and not args.no_cpu_baseline:
         cgbs, cdt, sample, cores = _cpu_baseline(spec, inp)
         line["cpu_baseline"] = {"value": cgbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}

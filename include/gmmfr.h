@@ -49,8 +49,14 @@ typedef enum {
   GMMFR_ERR_DEVICE = 5       /* a device-side check failed; see gmmfr_check_device_errors */
 } gmmfr_status;
 
-/* FP8 element formats of x1 and x2 (section 3.1: FP8 E4M3/E5M2). */
-typedef enum { GMMFR_E4M3 = 0, GMMFR_E5M2 = 1 } gmmfr_fp8_format;
+/* Element formats of x1 and x2: FP8 E4M3/E5M2 (section 3.1), or FP4 E2M1 for the
+ * MXFP4 scenario (aclnn V3, Atlas 350) stored two codes per byte along the row's
+ * contiguous dimension (K for x1 and a transposed x2, N for a non-transposed x2),
+ * the even element in the low nibble; K, and N for a non-transposed E2M1 x2, even
+ * (aclnn: "k must be even; n even when x2 is not transposed").  E2M1 operands are
+ * expanded exactly to E4M3 (weights at preparation, tokens per call) and run on the
+ * FP8 block-scaled MMA. */
+typedef enum { GMMFR_E4M3 = 0, GMMFR_E5M2 = 1, GMMFR_E2M1 = 2 } gmmfr_fp8_format;
 
 /* Integer type of row_index: int64 as in the tensor table, or int32. */
 typedef enum { GMMFR_INDEX_I64 = 0, GMMFR_INDEX_I32 = 1 } gmmfr_index_type;
@@ -115,7 +121,8 @@ GMMFR_API gmmfr_status gmmfr_prepared_weights_size(const gmmfr_problem* problem,
  * swizzled layout the grouped GEMM streams (one 128-column x 128-K tile of FP8
  * weights followed by its 512 scale bytes), so that each tile is a single
  * contiguous HBM read.  Inputs as in section 3.1 (x2 [E,K,N] or [E,N,K]; scale
- * [(E,)ceil(K/64),N,2] or [(E,)N,ceil(K/64),2]).
+ * [(E,)ceil(K/64),N,2] or [(E,)N,ceil(K/64),2]); an E2M1 x2 is packed two codes
+ * per byte along its last dimension and is stored prepared as E4M3 codes.
  *   prepared        device buffer of at least gmmfr_prepared_weights_size bytes,
  *                   16-byte aligned, caller-owned; fully overwritten.
  * Enqueued on `stream`; the buffer stays valid as long as the caller keeps it.
@@ -126,15 +133,16 @@ GMMFR_API gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const
 /*
  * Workspace bytes one call needs (two-phase use as in aclnn's
  * GetWorkspaceSize/execute pair).  `have_prepared` = 0 adds room to prepare
- * the weights inside the call.  Host only; may query the current device's SM
- * count.  The workspace must be 256-byte aligned.
+ * the weights inside the call; an E2M1 x1 adds M*K bytes for its expansion to
+ * E4M3.  Host only; may query the current device's SM count.  The workspace
+ * must be 256-byte aligned.
  */
 GMMFR_API gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int have_prepared, size_t* bytes);
 
 /*
  * The operator.  Enqueues the whole computation on `stream`; never syncs and
  * never allocates.
- *   x1              [M,K] FP8 bytes, 16-byte aligned
+ *   x1              [M,K] FP8 bytes (E2M1: [M,K/2], two codes per byte), 16-byte aligned
  *   x2, scale       raw weights and their scales; read only when prepared == NULL
  *                   (they are then prepared into the workspace first)
  *   pertoken_scale  [M,ceil(K/64),2] E8M0 bytes
@@ -289,7 +297,8 @@ GMMFR_API const char* gmmfr_last_error(void);
  * kernels on its stream.  gmmfr_profile_end SYNCHRONISES the device, writes
  * ms[call * GMMFR_PROFILE_SLOTS + slot] (-1 where a slot's kernel did not run),
  * sets *n_calls, and stops recording.
- * Slots: 0 weight preparation inside the call, 1 deterministic-mode routing (row
+ * Slots: 0 input preparation inside the call (weight preparation when no prepared
+ * weights are given, E2M1 token expansion), 1 deterministic-mode routing (row
  * CSR of the tokens), 2 grouped GEMM with fused epilogue, 3 deterministic combine,
  * 4 the whole call (start of its first kernel to end of its last).
  */

@@ -45,8 +45,8 @@ gmmfr_status validate(const gmmfr_problem* p) {
   if (p->N < 0 || p->N >= (int64_t(1) << 31)) return fail(GMMFR_ERR_INVALID_ARG, "N=%lld out of range [0, 2^31)", (long long)p->N);
   if (p->E < 1 || p->E > kMaxExperts) return fail(GMMFR_ERR_INVALID_ARG, "E=%lld out of range [1, 1024]", (long long)p->E);
   if (p->batch < 0 || p->batch >= (int64_t(1) << 31)) return fail(GMMFR_ERR_INVALID_ARG, "batch=%lld out of range [0, 2^31)", (long long)p->batch);
-  if (p->x1_format != GMMFR_E4M3 && p->x1_format != GMMFR_E5M2) return fail(GMMFR_ERR_INVALID_ARG, "x1_format=%d is not E4M3 (0) or E5M2 (1)", p->x1_format);
-  if (p->x2_format != GMMFR_E4M3 && p->x2_format != GMMFR_E5M2) return fail(GMMFR_ERR_INVALID_ARG, "x2_format=%d is not E4M3 (0) or E5M2 (1)", p->x2_format);
+  if (p->x1_format < GMMFR_E4M3 || p->x1_format > GMMFR_E2M1) return fail(GMMFR_ERR_INVALID_ARG, "x1_format=%d is not E4M3 (0), E5M2 (1) or E2M1 (2)", p->x1_format);
+  if (p->x2_format < GMMFR_E4M3 || p->x2_format > GMMFR_E2M1) return fail(GMMFR_ERR_INVALID_ARG, "x2_format=%d is not E4M3 (0), E5M2 (1) or E2M1 (2)", p->x2_format);
   if (p->transpose_x2 != 0 && p->transpose_x2 != 1) return fail(GMMFR_ERR_INVALID_ARG, "transpose_x2 must be 0 or 1");
   if (p->scale_per_expert != 0 && p->scale_per_expert != 1) return fail(GMMFR_ERR_INVALID_ARG, "scale_per_expert must be 0 or 1");
   if (p->group_list_type != 0 && p->group_list_type != 1) return fail(GMMFR_ERR_INVALID_ARG, "group_list_type=%d is not 0 (prefix sums) or 1 (counts)", p->group_list_type);
@@ -59,6 +59,8 @@ gmmfr_status validate(const gmmfr_problem* p) {
   if (p->flags & ~GMMFR_DETERMINISTIC) return fail(GMMFR_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
   if (p->expected_tokens_per_expert < 0)
     return fail(GMMFR_ERR_INVALID_ARG, "expected_tokens_per_expert=%lld is negative", (long long)p->expected_tokens_per_expert);
+  if (p->x2_format == GMMFR_E2M1 && !p->transpose_x2 && p->N % 2 != 0)
+    return fail(GMMFR_ERR_INVALID_ARG, "N=%lld: an E2M1 x2 that is not transposed needs an even N", (long long)p->N);
   if (p->K % 16 != 0) return fail(GMMFR_ERR_UNSUPPORTED, "K=%lld: this build needs K %% 16 == 0 (x1 rows are moved by TMA)", (long long)p->K);
   return GMMFR_OK;
 }
@@ -83,7 +85,7 @@ int fixed_tmax() {
 struct Layout {
   int64_t NT, KB, Ks;
   int split;
-  size_t off_cnt, off_rowptr, off_cursor, off_sorted, off_y, off_prep, total;
+  size_t off_cnt, off_rowptr, off_cursor, off_sorted, off_y, off_prep, off_tok, total;
 };
 
 Layout make_layout(const gmmfr_problem* p, bool have_prepared) {
@@ -114,6 +116,10 @@ Layout make_layout(const gmmfr_problem* p, bool have_prepared) {
   if (!have_prepared) {
     L.off_prep = off;
     off = align256(off + (size_t)p->E * L.NT * L.KB * gmmfr::kPrepTileBytes);
+  }
+  if (p->x1_format == GMMFR_E2M1) {  // E2M1 tokens expanded to E4M3 codes, [M, K] bytes
+    L.off_tok = off;
+    off = align256(off + (size_t)p->M * p->K);
   }
   L.total = off;
   return L;
@@ -198,6 +204,7 @@ static gmmfr::PrepParams prep_params(const gmmfr_problem* p, const void* x2, con
   pp.Ks = (int32_t)cdiv(p->K, 64);
   pp.transpose_x2 = p->transpose_x2;
   pp.scale_per_expert = p->scale_per_expert;
+  pp.fp4 = p->x2_format == GMMFR_E2M1;
   return pp;
 }
 
@@ -255,13 +262,19 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
 
   const uint8_t* wprep = static_cast<const uint8_t*>(prepared);
   timer.begin(4, s);
+  const bool fp4_tokens = p.x1_format == GMMFR_E2M1 && p.M > 0;
+  if (!prepared || fp4_tokens) timer.begin(0, s);
   if (!prepared) {
-    timer.begin(0, s);
     e = gmmfr::launch_prep(prep_params(problem, x2, scale, ws + L.off_prep), s);
-    timer.end(0, s);
     if (e != cudaSuccess) return cuda_fail(e, "weight preparation launch");
     wprep = ws + L.off_prep;
   }
+  if (fp4_tokens) {  // tokens: E2M1 -> E4M3, exact
+    e = gmmfr::launch_expand_fp4(static_cast<const uint8_t*>(x1), ws + L.off_tok, p.M * p.K / 2, s);
+    if (e != cudaSuccess) return cuda_fail(e, "token FP4 expansion launch");
+    x1 = ws + L.off_tok;
+  }
+  if (!prepared || fp4_tokens) timer.end(0, s);
 
   // x1 [M, K] bytes as 2-D tensors of 128-byte rows: boxes of 16, 32, 64, 128 rows, 128-byte swizzle
   gmmfr::TokenMaps tmaps;
@@ -330,8 +343,10 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   gp.deterministic = det;
   gp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;
   // instruction descriptor: A = weights (x2 format), B = tokens (x1 format),
-  // E8M0 scales (bit 23), M = 128 (bits 24..28 hold M >> 4)
-  gp.idesc = (1u << 23) | ((uint32_t)p.x2_format << 7) | ((uint32_t)p.x1_format << 10) | ((128u >> 4) << 24);
+  // E8M0 scales (bit 23), M = 128 (bits 24..28 hold M >> 4); E2M1 operands arrive expanded to E4M3
+  const uint32_t afmt = p.x2_format == GMMFR_E2M1 ? GMMFR_E4M3 : (uint32_t)p.x2_format;
+  const uint32_t bfmt = p.x1_format == GMMFR_E2M1 ? GMMFR_E4M3 : (uint32_t)p.x1_format;
+  gp.idesc = (1u << 23) | (afmt << 7) | (bfmt << 10) | ((128u >> 4) << 24);
   gp.timeout_ns = 4000000000ll;
   gp.test_stall = 0;
   if (const char* t = std::getenv("GMMFR_TEST_STALL_NS")) {  // testing aid: bounded-wait timeout path

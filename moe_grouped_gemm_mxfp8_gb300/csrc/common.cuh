@@ -36,7 +36,9 @@ struct PrepParams {
   int32_t NT, KB, Ks;
   int32_t transpose_x2;
   int32_t scale_per_expert;
+  int32_t fp4;  // x2 holds packed E2M1 codes: expand to E4M3
 };
+cudaError_t launch_expand_fp4(const uint8_t* packed, uint8_t* fp8, int64_t n_bytes, cudaStream_t s);
 
 // Deterministic mode: tokens of each out row (CSR, unordered within a row).
 struct CsrParams {

@@ -6,6 +6,63 @@
 
 namespace gmmfr {
 
+// ============================================================================ FP4 expansion
+// E2M1 code -> the E4M3 code of the same value (0, 0.5, 1, 1.5, 2, 3, 4, 6; sign in bit 3 -> bit 7).
+// Every E2M1 value is exactly an E4M3 value, so the expansion is exact.
+__device__ __forceinline__ uint8_t e2m1_to_e4m3(uint32_t c) {
+  constexpr uint32_t kLo = 0x3C383000u, kHi = 0x4C484440u;  // codes 0..3 and 4..7, one per byte
+  const uint32_t m = c & 7;
+  const uint32_t v = ((m < 4 ? kLo : kHi) >> (8 * (m & 3))) & 0xFFu;
+  return (uint8_t)(v | ((c & 8) << 4));
+}
+
+// packed [n_bytes] (two codes per byte, even element low) -> fp8 [2 * n_bytes]
+// n_vec: leading bytes handled 16 at a time (0 when either pointer is not 16-byte aligned)
+__global__ void __launch_bounds__(256) expand_fp4_kernel(const uint8_t* packed, uint8_t* fp8, int64_t n_bytes,
+                                                         int64_t n_vec) {
+  const int64_t n16 = n_vec / 16;
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n16; i += (int64_t)gridDim.x * 256) {
+    const uint4 in = reinterpret_cast<const uint4*>(packed)[i];
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t byte = (w[q] >> (8 * b)) & 0xFFu;
+        lo |= (uint32_t)e2m1_to_e4m3(byte & 15) << (16 * b);
+        lo |= (uint32_t)e2m1_to_e4m3(byte >> 4) << (16 * b + 8);
+        const uint32_t byte2 = (w[q] >> (8 * (b + 2))) & 0xFFu;
+        hi |= (uint32_t)e2m1_to_e4m3(byte2 & 15) << (16 * b);
+        hi |= (uint32_t)e2m1_to_e4m3(byte2 >> 4) << (16 * b + 8);
+      }
+      o[2 * q] = lo;
+      o[2 * q + 1] = hi;
+    }
+    reinterpret_cast<uint4*>(fp8)[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(fp8)[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  for (int64_t i = n16 * 16 + (int64_t)blockIdx.x * 256 + threadIdx.x; i < n_bytes; i += (int64_t)gridDim.x * 256) {
+    const uint32_t byte = packed[i];
+    fp8[2 * i] = e2m1_to_e4m3(byte & 15);
+    fp8[2 * i + 1] = e2m1_to_e4m3(byte >> 4);
+  }
+}
+
+cudaError_t launch_expand_fp4(const uint8_t* packed, uint8_t* fp8, int64_t n_bytes, cudaStream_t s) {
+  if (n_bytes == 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool vec = ((reinterpret_cast<uintptr_t>(packed) | reinterpret_cast<uintptr_t>(fp8)) & 15) == 0;
+  const int64_t n_vec = vec ? n_bytes / 16 * 16 : 0;
+  const int64_t work = vec ? n_vec / 16 + (n_bytes - n_vec) : n_bytes;
+  const int64_t blocks = (work + 255) / 256;
+  expand_fp4_kernel<<<(unsigned)(blocks < sms * 4 ? blocks : sms * 4), 256, 0, s>>>(packed, fp8, n_bytes, n_vec);
+  return cudaGetLastError();
+}
+
 // ============================================================================ weight prep
 // Prepared tile (e, j, kb): 128 output columns n = j*128 + r by 128 K bytes
 // k = kb*128 + c, stored as the shared-memory image of a K-major operand with
@@ -29,7 +86,20 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepParams p) {
       const int64_t n = j * kTileN + r;
       const int64_t k0 = kb * kTileK + c * 16;
       uint8_t b[16];
-      if (p.transpose_x2) {  // x2 [E, N, K]: the 16 bytes are contiguous
+      if (p.fp4) {  // packed E2M1: along K (transposed) or along N (not transposed)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          uint8_t v = 0;
+          const int64_t k = k0 + i;
+          if (n < p.N && k < p.K) {
+            const uint32_t byte = p.transpose_x2 ? p.x2[(e * p.N + n) * (p.K / 2) + k / 2]
+                                                 : p.x2[(e * p.K + k) * (p.N / 2) + n / 2];
+            const int hi = p.transpose_x2 ? (int)(k & 1) : (int)(n & 1);
+            v = e2m1_to_e4m3(hi ? byte >> 4 : byte & 15);
+          }
+          b[i] = v;
+        }
+      } else if (p.transpose_x2) {  // x2 [E, N, K]: the 16 bytes are contiguous
         const uint8_t* src = p.x2 + (e * p.N + n) * p.K + k0;
         if (n < p.N && k0 + 16 <= p.K && ((reinterpret_cast<uintptr_t>(src) & 15) == 0)) {
           *reinterpret_cast<uint4*>(b) = *reinterpret_cast<const uint4*>(src);

@@ -34,6 +34,7 @@ import torch
 
 E4M3 = 0
 E5M2 = 1
+E2M1 = 2  # OCP FP4, two codes per byte along the contiguous dimension, even element in the low nibble
 
 _TORCH_FP8 = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
 
@@ -121,6 +122,11 @@ def group_list_from_counts(counts: torch.Tensor, group_list_type: int) -> torch.
 
 
 def _fp8_bytes(shape, dtype_code: int, g: torch.Generator, device: str) -> torch.Tensor:
+    """FP8: randn cast to the format.  E2M1: uniformly random 4-bit codes, two per byte
+    along the last dimension (shape is the logical shape; its last size must be even)."""
+    if dtype_code == E2M1:
+        packed = tuple(shape[:-1]) + (shape[-1] // 2,)
+        return torch.randint(0, 256, packed, generator=g, device=device, dtype=torch.int32).to(torch.uint8)
     x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
     return x.to(_TORCH_FP8[dtype_code]).view(torch.uint8)
 
@@ -227,6 +233,12 @@ def config(i: int) -> Spec:
     raise ValueError(i)
 
 
+def mxfp4_config() -> Spec:
+    """The large workload (5) with MXFP4 (E2M1) tokens and weights."""
+    return dataclasses.replace(config(5), name="C5-MXFP4 M4096 K7168 N4096 E256", x1_dtype=E2M1, x2_dtype=E2M1,
+                               seed=1105)
+
+
 def algorithmic_bytes(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:
     """Bytes a single call must move at minimum: x2 (and its scales) of every
     expert that holds a token, x1, pertoken_scale, logit, row_index,
@@ -236,8 +248,9 @@ def algorithmic_bytes(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:
     nnz = int((counts > 0).sum())
     covered = min(int(counts.sum()), spec.M)
     K, N, Ks = spec.K, spec.N, spec.Ks
-    w = nnz * K * N + nnz * Ks * N * 2 if spec.scale_per_expert else nnz * K * N + Ks * N * 2
-    tok = covered * K + covered * Ks * 2 + covered * 4 * (0 if spec.logit == "none" else 1) + covered * 8
+    wb = K * N // 2 if spec.x2_dtype == E2M1 else K * N
+    w = nnz * wb + nnz * Ks * N * 2 if spec.scale_per_expert else nnz * wb + Ks * N * 2
+    tok = covered * (K // 2 if spec.x1_dtype == E2M1 else K) + covered * Ks * 2 + covered * 4 * (0 if spec.logit == "none" else 1) + covered * 8
     shared = spec.n_shared * N * 2
     out = spec.batch * N * 4 * 2
     return w + tok + shared + out + spec.E * 8

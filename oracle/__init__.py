@@ -110,7 +110,9 @@ class Problem:
             logit=_np(logit, np.float32), rows=_np(row_index, np.int64),
             shared=_np(shared_input, np.uint16), out=_np(out, np.float32), bias=_np(bias, np.uint16))
         k = self.keep
-        assert k["x1"].size == M * K and k["x2"].size == E * K * N
+        p1 = 2 if int(x1_dtype) == 2 else 1
+        p2 = 2 if int(x2_dtype) == 2 else 1
+        assert k["x1"].size == M * K // p1 and k["x2"].size == E * K * N // p2
         assert k["out"].size == batch * N and k["rows"].size == M and k["gl"].size == E
         shared_rows = 0 if k["shared"] is None else k["shared"].size // max(N, 1)
 

@@ -36,6 +36,9 @@
  *     weighting: out[row_index[t], n] += logit[t] * (acc(t,n) + bias[e,n]);
  *   - logit == NULL means weight 1 (has_logit=False, section 5.3);
  *     shared_input == NULL skips stage 4;
+ *   - MXFP4 (aclnn V3, Atlas 350 MX scenarios): x1 and x2 hold E2M1 codes two per
+ *     byte along the contiguous dimension, the even element in the low nibble
+ *     (reading); scales are the same E8M0 per 32 elements;
  *   - contributions are added in ascending token order, the shared term last
  *     (the golden's per-expert index_add_ followed by the shared add, section 6.3).
  *
@@ -81,8 +84,24 @@ static double decode_e5m2(uint32_t b) {
   return s ? -v : v;
 }
 
+/* OCP FP4 E2M1: sign, 2 exponent bits with bias 1, 1 mantissa bit; exponent 0 is
+ * subnormal (m * 0.5); no Inf or NaN; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+static double decode_e2m1(uint32_t b) {
+  const int s = (b >> 3) & 1, e = (b >> 1) & 3, m = b & 1;
+  const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -v : v;
+}
+
 double oracle_decode_fp8(int fmt, uint32_t code) {
+  if (fmt == ORACLE_E2M1) return decode_e2m1(code & 15);
   return fmt == ORACLE_E5M2 ? decode_e5m2(code & 255) : decode_e4m3fn(code & 255);
+}
+
+/* element i of a row stored with `fmt` (two E2M1 codes per byte, even element low) */
+static uint32_t element_code(const uint8_t* row, int64_t i, int fmt) {
+  if (fmt != ORACLE_E2M1) return row[i];
+  const uint8_t b = row[i / 2];
+  return (i & 1) ? (b >> 4) : (b & 15);
 }
 
 /* OCP MX scale E8M0: 2^(b - 127); 0xFF is NaN. */
@@ -140,22 +159,24 @@ static int64_t scale_index(const oracle_args* a, int64_t e, int64_t k, int64_t n
   return base + ((k / 64) * a->N + n) * 2 + (k / 32) % 2;
 }
 
-static int64_t x2_index(const oracle_args* a, int64_t e, int64_t k, int64_t n) {
-  if (a->transpose_x2) return (e * a->N + n) * a->K + k;
-  return (e * a->K + k) * a->N + n;
+static uint32_t x2_code(const oracle_args* a, int64_t e, int64_t k, int64_t n) {
+  const int p = a->x2_fmt == ORACLE_E2M1 ? 2 : 1;  /* elements per byte */
+  if (a->transpose_x2) return element_code(a->x2 + (e * a->N + n) * (a->K / p), k, a->x2_fmt);
+  return element_code(a->x2 + (e * a->K + k) * (a->N / p), n, a->x2_fmt);
 }
 
 /* A(t,k): token value times its block scale */
 static double token_value(const oracle_args* a, int64_t t, int64_t k) {
   const int64_t Ks = (a->K + 63) / 64;
-  const double v = oracle_decode_fp8(a->x1_fmt, a->x1[t * a->K + k]);
+  const int p = a->x1_fmt == ORACLE_E2M1 ? 2 : 1;
+  const double v = oracle_decode_fp8(a->x1_fmt, element_code(a->x1 + t * (a->K / p), k, a->x1_fmt));
   const double s = oracle_decode_e8m0(a->pertoken_scale[(t * Ks + k / 64) * 2 + (k / 32) % 2]);
   return v * s;
 }
 
 /* B(e,k,n): weight value times its block scale */
 static double weight_value(const oracle_args* a, int64_t e, int64_t k, int64_t n) {
-  const double v = oracle_decode_fp8(a->x2_fmt, a->x2[x2_index(a, e, k, n)]);
+  const double v = oracle_decode_fp8(a->x2_fmt, x2_code(a, e, k, n));
   const double s = oracle_decode_e8m0(a->scale[scale_index(a, e, k, n)]);
   return v * s;
 }

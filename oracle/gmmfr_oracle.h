@@ -17,7 +17,10 @@
 extern "C" {
 #endif
 
-enum { ORACLE_E4M3 = 0, ORACLE_E5M2 = 1 };
+/* element formats; E2M1 (OCP FP4) is stored two per byte, the even element in
+ * the low nibble, along the row's contiguous dimension (K for x1 and a
+ * transposed x2, N for a non-transposed x2) */
+enum { ORACLE_E4M3 = 0, ORACLE_E5M2 = 1, ORACLE_E2M1 = 2 };
 
 /* error flags returned by the oracle (the readings of invalid input) */
 enum {

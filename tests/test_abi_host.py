@@ -59,7 +59,8 @@ BAD = [
     (dict(K=0), B.ERR_INVALID_ARG, "K=0"),
     (dict(N=-5), B.ERR_INVALID_ARG, "N=-5"),
     (dict(batch=-1, shared_rows=0), B.ERR_INVALID_ARG, "batch=-1"),
-    (dict(x1_format=2), B.ERR_INVALID_ARG, "x1_format"),
+    (dict(x1_format=3), B.ERR_INVALID_ARG, "x1_format"),
+    (dict(x2_format=2, N=63), B.ERR_INVALID_ARG, "even N"),
     (dict(x2_format=7), B.ERR_INVALID_ARG, "x2_format"),
     (dict(group_list_type=2), B.ERR_INVALID_ARG, "group_list_type"),
     (dict(row_index_type=5), B.ERR_INVALID_ARG, "row_index_type"),
@@ -134,6 +135,19 @@ def test_sizes_follow_the_tiling(lib):
         assert without - with_prep >= s.E * nt * kb * 16896
         pd = B.problem_from_spec(s, deterministic=True)
         assert B.gmmfr_workspace_size(pd, True) >= with_prep + 4 * s.M * s.N
+
+
+def test_e2m1_sizes_and_parity_rules(lib):
+    """MXFP4: an odd N is allowed when x2 is transposed (packed along K); E2M1
+    tokens add M*K bytes of workspace for their E4M3 expansion; the prepared
+    weights are the FP8 tiles whatever the input format."""
+    base = _ok_problem()
+    n8 = B.gmmfr_workspace_size(base, True)
+    p4 = _ok_problem(x1_format=2, x2_format=2)
+    assert B.gmmfr_workspace_size(p4, True) >= n8 + p4.M * p4.K
+    assert B.gmmfr_prepared_weights_size(p4) == B.gmmfr_prepared_weights_size(base)
+    B.gmmfr_workspace_size(_ok_problem(x2_format=2, N=63, transpose_x2=1), True)
+    B.gmmfr_workspace_size(_ok_problem(x1_format=2, N=63), True)
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):

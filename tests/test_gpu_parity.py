@@ -156,6 +156,16 @@ SMALL = {
     "bias_split_k": dict(E=4, M=60, N=320, K=1024, bias=True, rows="random", out_init="randn"),
     "bias_wide": dict(E=3, M=300, batch=64, N=256, K=256, bias=True, counts="explicit",
                       explicit_counts=(150, 0, 150), rows="random", transpose_x2=True),
+    # MXFP4 (E2M1 codes two per byte, expanded exactly to E4M3 before the MMA)
+    "mxfp4": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1),
+    "mxfp4_t": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, transpose_x2=True, rows="random"),
+    "mxfp4_tokens_e5m2_weights": dict(x1_dtype=W.E2M1, x2_dtype=W.E5M2, K=96),
+    "e4m3_tokens_mxfp4_weights": dict(x2_dtype=W.E2M1, transpose_x2=True, scale_per_expert=True, bias=True,
+                                      N=255),
+    "mxfp4_k16_n2": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, K=16, N=2, M=7, batch=5),  # 56-byte packed x1
+    "mxfp4_straddle": dict(E=9, M=1344, batch=200, N=256, K=128, rows="random", x1_dtype=W.E2M1,
+                           x2_dtype=W.E2M1, counts="explicit",
+                           explicit_counts=(63, 64, 65, 127, 128, 129, 255, 256, 257)),
 }
 
 
@@ -165,7 +175,7 @@ def test_small_atomic(name):
 
 
 @pytest.mark.parametrize("name", ["basic", "transposed", "ragged_counts", "random_rows_shared", "straddle", "k96",
-                                  "bias_split_k"])
+                                  "bias_split_k", "mxfp4_t"])
 def test_small_deterministic(name):
     spec = _spec(**SMALL[name])
     inp = W.make_inputs(spec)
@@ -298,6 +308,24 @@ def test_config_sampled(i):
     inp = W.make_inputs(spec, weights_device="cuda")
     inp["x2"] = inp["x2"].cpu()
     check_sampled(spec, inp)
+
+
+def test_mxfp4_large_sampled():
+    spec = W.mxfp4_config()
+    inp = W.make_inputs(spec, weights_device="cuda")
+    inp["x2"] = inp["x2"].cpu()
+    check_sampled(spec, inp)
+
+
+def test_mxfp4_raw_weights_in_call():
+    """E2M1 weights prepared inside the call (no prepared buffer)."""
+    spec = _spec(**SMALL["mxfp4_t"])
+    inp = W.make_inputs(spec)
+    got, bits = gpu_run(spec, inp, prepared=False)
+    ref, absb, flags = oracle.run(oracle.problem_from_spec(spec, inp))
+    init, sh = _extra_terms(spec, inp)
+    assert_close(got, ref, oracle.tolerance(ref, absb, init, sh))
+    assert bits == flags
 
 
 def test_config4_deterministic_bit_stable():

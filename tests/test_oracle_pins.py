@@ -70,6 +70,26 @@ def test_bf16_decode_matches_torch():
     assert np.array_equal(ref, got)
 
 
+# OCP Microscaling Formats (MX) v1.0, FP4 E2M1 element table: codes 0..7 are
+# 0, 0.5, 1, 1.5, 2, 3, 4, 6; codes 8..15 the same magnitudes negated.
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_e2m1_decode_matches_ocp_table():
+    got = [oracle.decode_fp8(W.E2M1, c) for c in range(16)]
+    assert got == E2M1_VALUES
+    assert [math.copysign(1.0, v) for v in got[8:]] == [-1.0] * 8  # the sign bit of -0 too
+    # only the low nibble is a code: higher bits of the byte are ignored
+    assert [oracle.decode_fp8(W.E2M1, 0xF0 | c) for c in range(16)] == E2M1_VALUES
+
+
+def test_every_e2m1_value_is_an_e4m3_value():
+    """Each FP4 value is exactly representable in E4M3, so an FP4 problem equals
+    the same problem with its codes widened to E4M3 bytes."""
+    vals = torch.tensor(E2M1_VALUES, dtype=torch.float64)
+    assert torch.equal(vals.to(torch.float8_e4m3fn).to(torch.float64), vals)
+
+
 # ----------------------------------------------------------------------------- helpers
 def _spec(**kw) -> W.Spec:
     base = dict(name="tiny", batch=4, M=12, K=128, N=24, E=3, seed=7)
@@ -88,8 +108,16 @@ def _torch_golden(spec: W.Spec, inp) -> np.ndarray:
     then add the weighted shared input."""
     M, K, N, E = spec.M, spec.K, spec.N, spec.E
     f8 = {W.E4M3: torch.float8_e4m3fn, W.E5M2: torch.float8_e5m2}
-    x1 = inp["x1"].view(f8[spec.x1_dtype]).to(torch.float64)
-    x2 = inp["x2"].view(f8[spec.x2_dtype]).to(torch.float64)
+
+    def decode(t, fmt):
+        if fmt != W.E2M1:
+            return t.view(f8[fmt]).to(torch.float64)
+        # unpack the nibbles (even element low) and look them up in the OCP FP4 table
+        codes = torch.stack([t & 15, t >> 4], dim=-1).reshape(*t.shape[:-1], -1).long()
+        return torch.tensor(E2M1_VALUES, dtype=torch.float64)[codes]
+
+    x1 = decode(inp["x1"], spec.x1_dtype)
+    x2 = decode(inp["x2"], spec.x2_dtype)
     if spec.transpose_x2:
         x2 = x2.transpose(1, 2)  # -> [E, K, N]
     e8 = lambda b: b.view(torch.float8_e8m0fnu).to(torch.float64)
@@ -242,6 +270,10 @@ TINY = [
     dict(logit="none", shared_rows=0),
     dict(bias=True, rows="random", out_init="randn"),
     dict(bias=True, transpose_x2=True, counts="explicit", explicit_counts=(0, 7, 5), M=14),
+    dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1),                       # MXFP4, x2 packed along N
+    dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, transpose_x2=True),    # x2 packed along K
+    dict(x1_dtype=W.E2M1, x2_dtype=W.E4M3, K=96, rows="random"),
+    dict(x1_dtype=W.E5M2, x2_dtype=W.E2M1, transpose_x2=True, scale_per_expert=True, bias=True),
 ]
 
 
@@ -253,6 +285,31 @@ def test_brute_force_against_torch_golden(kw):
     ref = _torch_golden(spec, inp)
     assert flags == 0
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("transpose", [False, True])
+def test_e2m1_problem_equals_its_e4m3_widening(transpose):
+    """Packed FP4 inputs and the same values widened to one E4M3 byte each give
+    bit-identical oracle results (exact values, same summation order).  The
+    widening unpacks with numpy along each tensor's last dimension, so a swapped
+    nibble order or a packing along the wrong dimension in the oracle fails."""
+    spec = _spec(x1_dtype=W.E2M1, x2_dtype=W.E2M1, transpose_x2=transpose, rows="random", out_init="randn")
+    inp = W.make_inputs(spec)
+    out4, absb4, f4 = _run(spec, inp)
+
+    def widen(t):
+        a = t.numpy()
+        codes = np.stack([a & 15, a >> 4], axis=-1).reshape(*a.shape[:-1], -1)
+        vals = torch.from_numpy(np.array(E2M1_VALUES)[codes])
+        return vals.to(torch.float8_e4m3fn).view(torch.uint8)
+
+    spec8 = dataclasses.replace(spec, x1_dtype=W.E4M3, x2_dtype=W.E4M3)
+    inp8 = dict(inp, x1=widen(inp["x1"]), x2=widen(inp["x2"]))
+    out8, absb8, f8 = _run(spec8, inp8)
+    assert f4 == f8 == 0
+    assert np.array_equal(out4, out8) and np.array_equal(absb4, absb8)
+    # and the FP4 codes do reach every value of the table
+    assert set(np.unique(inp["x1"].numpy() & 15)) == set(range(16))
 
 
 # ----------------------------------------------------------------------------- routing pins
