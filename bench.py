@@ -451,9 +451,10 @@ def run_ours(args):
         "clocks": clk.summary(),
         "wall_s_timed": t_wall,
     }
-    line["route"] = _time_route(args, flush)
-    line["ffn"] = _time_ffn(args, flush)
-    line["mxfp4"] = _time_mxfp4(args, flush)
+    if not args.no_extras:
+        line["route"] = _time_route(args, flush)
+        line["ffn"] = _time_ffn(args, flush)
+        line["mxfp4"] = _time_mxfp4(args, flush)
     if rank == 0 and not args.no_cpu_baseline:
         cgbs, cdt, sample, cores = _cpu_baseline(spec, inp)
         line["cpu_baseline"] = {"value": cgbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
@@ -472,6 +473,8 @@ def main():
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the side measurements (routing step, SwiGLU FFN, MXFP4 operator)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
