@@ -185,9 +185,10 @@ def test_small_deterministic(name):
 
 
 @pytest.mark.parametrize("tmax", ["32", "64", "128"])
-def test_token_group_widths(tmax, monkeypatch):
+@pytest.mark.parametrize("case", ["straddle", "mxfp4_straddle"])
+def test_token_group_widths(tmax, case, monkeypatch):
     monkeypatch.setenv("GMMFR_TMAX", tmax)
-    spec = _spec(**SMALL["straddle"])
+    spec = _spec(**SMALL[case])
     check_full(spec, W.make_inputs(spec))
 
 
@@ -282,6 +283,25 @@ def test_prepared_layout_round_trip():
                     sv = sc[kp, nn, h] if not transpose else sc[nn, kp, h]
                     exp_s = np.where(((j * 128 + r) < N) & (g * 32 < K), sv, 127)
                     assert np.array_equal(s, exp_s)
+
+
+def test_prepared_e2m1_equals_prepared_e4m3_widening():
+    """E2M1 weights are prepared as the E4M3 tiles of the same values: the prepared
+    buffer of packed FP4 x2 is byte-identical to that of x2 widened to one E4M3
+    byte per element (the widening done here with torch's float8 cast)."""
+    table = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+    for transpose in (False, True):
+        spec = _spec(K=208, N=200, E=2, transpose_x2=transpose, x1_dtype=W.E2M1, x2_dtype=W.E2M1)
+        inp = W.make_inputs(spec)
+        x2 = inp["x2"]
+        codes = torch.stack([x2 & 15, x2 >> 4], dim=-1).reshape(*x2.shape[:-1], -1).long()
+        wide = table[codes].to(torch.float8_e4m3fn).view(torch.uint8)
+        prob4 = B.problem_from_spec(spec)
+        prob8 = B.problem_from_spec(dataclasses.replace(spec, x1_dtype=W.E4M3, x2_dtype=W.E4M3))
+        sc = inp["scale"].cuda()
+        p4 = B.prepare_weights(prob4, x2.cuda(), sc).cpu()
+        p8 = B.prepare_weights(prob8, wide.cuda(), sc).cpu()
+        assert p4.numel() == p8.numel() and torch.equal(p4, p8)
 
 
 def test_timeout_path_reports_and_recovers(monkeypatch):
