@@ -80,6 +80,7 @@ struct Sched {
   int64_t i, i_end, step;
   int NT, KB, split, ng;
   bool det;
+  bool small;  // the whole iteration space fits 31 bits: 32-bit index arithmetic
   __device__ void init(int n_groups, int NT_, int KB_, bool det_, int split_) {
     ng = n_groups;
     NT = NT_;
@@ -97,9 +98,22 @@ struct Sched {
       i_end = tiles * split;
       step = gridDim.x;
     }
+    small = i_end + step < ((int64_t)1 << 31);
   }
   __device__ bool next(Seg& s) {
     if (i >= i_end) return false;
+    if (small && !det) {  // the common case, without 64-bit divisions
+      const uint32_t i32 = (uint32_t)i, kb = (uint32_t)KB;
+      const uint32_t tile = i32 / kb;
+      s.kb0 = (int)(i32 - tile * kb);
+      const uint32_t left = (uint32_t)(i_end - i);
+      s.kb1 = (kb - s.kb0) < left ? (int)kb : s.kb0 + (int)left;
+      i += s.kb1 - s.kb0;
+      s.slot = 0;
+      s.g = (int)(tile % (uint32_t)ng);
+      s.j = (int)(tile / (uint32_t)ng);
+      return true;
+    }
     int64_t tile;
     if (!det) {
       tile = i / KB;
@@ -154,7 +168,9 @@ __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uin
 // type 0 prefix sums, type 1 counts),
 // made contiguous and clamped to [0, M]; sets kErrBadGroupList when clamping was
 // needed.  Fills s_end, chooses tmax, fills s_gbase.  Returns the group count.
-__device__ int decode_groups(const GemmParams& p, int32_t* s_end, int32_t* s_gbase, int64_t* scratch,
+// g0 = group_list[threadIdx.x] (0 past E), loaded by the caller at kernel entry so that
+// its latency overlaps the barrier and TMEM set-up.
+__device__ int decode_groups(const GemmParams& p, int64_t g0, int32_t* s_end, int32_t* s_gbase, int64_t* scratch,
                              uint32_t* s_err, int& tmax_out) {
   const int E = p.E;
   const int64_t M = p.M;
@@ -162,7 +178,7 @@ __device__ int decode_groups(const GemmParams& p, int32_t* s_end, int32_t* s_gba
   int64_t carry = 0;
   for (int base = 0; base < E; base += kGemmThreads) {  // uniform trip count
     const int e = base + tid;
-    const int64_t g = e < E ? p.group_list[e] : 0;
+    const int64_t g = base == 0 ? g0 : (e < E ? p.group_list[e] : 0);
     int64_t v, tot;
     if (p.group_list_type == 1) {
       if (e < E && g < 0) atomicOr(s_err, kErrBadGroupList);
@@ -298,6 +314,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* s_err = reinterpret_cast<uint32_t*>(&misc[2]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t g0 = threadIdx.x < p.E ? p.group_list[threadIdx.x] : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < cfg::kMaxStages; ++s) {
@@ -321,7 +338,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   __syncthreads();
   int tmax;
-  const int n_groups = decode_groups(p, s_end, s_gbase, s_scan, s_err, tmax);
+  const int n_groups = decode_groups(p, g0, s_end, s_gbase, s_scan, s_err, tmax);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
