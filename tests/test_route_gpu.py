@@ -29,6 +29,8 @@ CASES = [
     dict(batch=1000, topk=1, K=128, E=1),
     dict(batch=777, topk=6, K=512, E=1024, invalid=1),
     dict(batch=0, topk=4, K=128, E=8),
+    dict(batch=2048, topk=4, K=8192, E=256),                   # 8192 entries: the largest single-launch case
+    dict(batch=3001, topk=4, K=144, E=64, invalid=5),          # 12004 entries: the three-launch path
 ]
 
 
@@ -42,6 +44,24 @@ def test_route_bit_exact(kw, ids32, glt):
                       inp["x_scale"].numpy(), spec.E, glt)
     ids = inp["topk_ids"].to(torch.int32) if ids32 else inp["topk_ids"]
     out, ws = B.route(ids.cuda(), inp["topk_weights"].cuda(), inp["x"].cuda(), inp["x_scale"].cuda(), spec.E, glt)
+    bits = B.gmmfr_check_device_errors(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert bits == (B.DEV_BAD_EXPERT_ID if ref["flags"] else 0)
+    for k in ("perm", "x1", "pertoken_scale", "group_list", "row_index", "logit"):
+        got = out[k].cpu().numpy()
+        assert np.array_equal(got.reshape(ref[k].shape).astype(ref[k].dtype), ref[k]), k
+
+
+@pytest.mark.parametrize("kw", [CASES[1], CASES[2], CASES[4], CASES[5]], ids=["1", "2", "4", "5"])
+def test_route_three_launch_path_bit_exact(kw, monkeypatch):
+    """Below 8193 entries the library routes in one launch; the three-launch path
+    (count, scan, scatter) gives the same bytes."""
+    monkeypatch.setenv("GMMFR_ROUTE_SPLIT", "1")
+    spec = W.RouteSpec("t", seed=kw["batch"] + kw["E"], **kw)
+    inp = W.make_route_inputs(spec)
+    ref = R.moe_route(inp["topk_ids"].numpy(), inp["topk_weights"].numpy(), inp["x"].numpy(),
+                      inp["x_scale"].numpy(), spec.E, 1)
+    out, ws = B.route(inp["topk_ids"].cuda(), inp["topk_weights"].cuda(), inp["x"].cuda(), inp["x_scale"].cuda(),
+                      spec.E, 1)
     bits = B.gmmfr_check_device_errors(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert bits == (B.DEV_BAD_EXPERT_ID if ref["flags"] else 0)
     for k in ("perm", "x1", "pertoken_scale", "group_list", "row_index", "logit"):
