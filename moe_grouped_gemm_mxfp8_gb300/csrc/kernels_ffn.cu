@@ -240,7 +240,10 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
   const int stage_bytes = ffn::stage_bytes(tmax);
   const int n_stages = ffn::n_stages(tmax);
   const Ctl ctl{abort_flag, s_err, p.timeout_ns};
+  // units (group, column tile), column tile fastest, in one contiguous range per CTA: a CTA
+  // streams consecutive prepared tiles of one expert and re-reads that expert's token rows
   const int64_t n_units = (int64_t)n_groups * p.NT;
+  const int64_t u_begin = n_units * blockIdx.x / gridDim.x, u_end = n_units * (blockIdx.x + 1) / gridDim.x;
   const uint32_t smem_base = ptx::smem_u32(smem);
 
   if (warp == 0) {
@@ -254,8 +257,8 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const int g = (int)(u % n_groups), j = (int)(u / n_groups);
+      for (int64_t u = u_begin; ok && u < u_end; ++u) {
+        const int g = (int)(u / p.NT), j = (int)(u % p.NT);
         int e, t0, T;
         groups.info(g, e, t0, T);
         const int m = (T + 15) / 16;
@@ -307,8 +310,8 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
       uint32_t phase = 0;
       int acc_i = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const int g = (int)(u % n_groups);
+      for (int64_t u = u_begin; ok && u < u_end; ++u) {
+        const int g = (int)(u / p.NT);
         int e, t0, T;
         groups.info(g, e, t0, T);
         const uint32_t npad = (uint32_t)((T + 15) / 16) * 16;
@@ -348,8 +351,8 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     int acc_i = 0;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const int g = (int)(u % n_groups), j = (int)(u / n_groups);
+    for (int64_t u = u_begin; u < u_end; ++u) {
+      const int g = (int)(u / p.NT), j = (int)(u % p.NT);
       int e, t0, T;
       groups.info(g, e, t0, T);
       const int buf = acc_i & 1;
