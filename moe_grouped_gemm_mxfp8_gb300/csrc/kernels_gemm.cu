@@ -26,7 +26,9 @@
 //              the 32-row x 16-byte layout tcgen05.cp spreads over TMEM lanes.
 //
 // Scheduling: atomic mode splits the total (group, tile, K-block) iteration space
-// evenly over the CTAs (stream-K); a tile cut between CTAs is finished by
+// over the CTAs in contiguous ranges (stream-K) of equal item count, or, when token
+// groups of 64 or 128 are in play, of equal cost (item_cost: CTAs holding 128-token
+// groups get fewer items than those holding 16-token ones); a tile cut between CTAs is finished by
 // atomics, which is exact up to FP32 rounding order since every term is linear.
 // Deterministic mode gives each (group, tile, K-split) unit to one CTA and
 // stores its result for the row-ordered combine.
@@ -62,7 +64,8 @@ constexpr int kNumBars = 2 * kMaxStages + 6;
 constexpr int kBarOff = kArena;
 constexpr int kEndOff = kBarOff + kNumBars * 8;              // int32 s_end[1024]
 constexpr int kGbaseOff = kEndOff + 4 * kMaxExperts;         // int32 s_gbase[1025]
-constexpr int kScanOff = kGbaseOff + 4 * (kMaxExperts + 4);  // int64 scan scratch[8]
+constexpr int kWbaseOff = kGbaseOff + 4 * (kMaxExperts + 4); // int32 s_wbase[1025]
+constexpr int kScanOff = kWbaseOff + 4 * (kMaxExperts + 4);  // int64 scan scratch[8]
 constexpr int kMiscOff = kScanOff + 8 * 8;                   // int32 misc[8]
 constexpr int kSmemBytes = kMiscOff + 32 + 1024;             // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -70,6 +73,57 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Seg {
   int g, j, kb0, kb1, slot;
+};
+
+// Relative time of one (group, tile, K block) item of a group of T tokens: the prepared
+// weight tile with its scales (132 units of 128 bytes, from HBM) weighted 3:1 against the
+// token rows (16 at a time, mostly L2 hits, re-read by every column tile) — the ratio that
+// evened out per-CTA finish times on a Zipf routing with 1 to 128 tokens per group.
+__host__ __device__ constexpr int item_cost(int T) { return 3 * (kPrepTileBytes / 128) + 16 * ((T + 15) / 16); }
+
+// Expert ranges and token groups decoded from group_list, in shared memory.
+struct Groups {
+  const int32_t* end;    // end of expert e's token range (ranges are contiguous from 0)
+  const int32_t* gbase;  // first group of expert e; gbase[E] = number of groups
+  const int32_t* wbase;  // cost of the items of experts before e in one K block of one tile
+                         // (item_cost units); wbase[E] = total, < 0 when it would overflow
+  int E, tmax;
+  // group g -> expert, first token, tokens
+  __device__ void info(int g, int& e, int& t0, int& T) const {
+    int lo = 0, hi = E - 1;  // largest e with gbase[e] <= g (always a non-empty expert)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (gbase[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    const int start = lo ? end[lo - 1] : 0;
+    const int i = g - gbase[lo];
+    t0 = start + i * tmax;
+    const int rem = end[lo] - t0;
+    T = rem < tmax ? rem : tmax;
+  }
+  // First item (index tile * KB + kb, tile = j * n_groups + g) whose cost prefix reaches x.
+  __device__ int64_t item_at(int64_t x, int KB, int NT, int n_groups) const {
+    const int64_t row = (int64_t)KB * wbase[E];  // all items of one column tile
+    const int64_t j = x / row;
+    if (j >= NT) return (int64_t)n_groups * NT * KB;
+    const int64_t r = x - j * row;
+    int lo = 0, hi = E - 1;  // the last expert whose items start at or before r (it holds tokens)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)KB * wbase[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int ng = gbase[e + 1] - gbase[e];
+    const int64_t wf = item_cost(tmax);
+    const int64_t re = r - (int64_t)KB * wbase[e];
+    int64_t gl = re / ((int64_t)KB * wf);
+    if (gl > ng - 1) gl = ng - 1;
+    const int last_t = end[e] - (e ? end[e - 1] : 0) - (ng - 1) * tmax;
+    const int64_t wg = gl < ng - 1 ? wf : item_cost(last_t);
+    const int64_t rg = re - gl * KB * wf;
+    return (j * n_groups + gbase[e] + gl) * KB + (rg + wg - 1) / wg;  // kb == KB is the next tile
+  }
 };
 
 // The sequence of (group, tile, K range) segments of one CTA; every role walks it.
@@ -81,14 +135,20 @@ struct Sched {
   int NT, KB, split, ng;
   bool det;
   bool small;  // the whole iteration space fits 31 bits: 32-bit index arithmetic
-  __device__ void init(int n_groups, int NT_, int KB_, bool det_, int split_) {
+  __device__ void init(int n_groups, int NT_, int KB_, bool det_, int split_, const Groups& gr) {
     ng = n_groups;
     NT = NT_;
     KB = KB_;
     det = det_;
     split = split_;
     const int64_t tiles = (int64_t)n_groups * NT;
-    if (!det) {
+    if (!det && gr.wbase[gr.E] > 0) {
+      // equal cost per CTA: items of large token groups move more bytes than those of small ones
+      const int64_t total = (int64_t)NT * KB * gr.wbase[gr.E];
+      i = gr.item_at(total * blockIdx.x / gridDim.x, KB, NT, n_groups);
+      i_end = gr.item_at(total * (blockIdx.x + 1) / gridDim.x, KB, NT, n_groups);
+      step = 0;
+    } else if (!det) {
       const int64_t total = tiles * KB;
       i = total * blockIdx.x / gridDim.x;
       i_end = total * (blockIdx.x + 1) / gridDim.x;
@@ -136,27 +196,6 @@ struct Sched {
   }
 };
 
-// Expert ranges and token groups decoded from group_list, in shared memory.
-struct Groups {
-  const int32_t* end;    // end of expert e's token range (ranges are contiguous from 0)
-  const int32_t* gbase;  // first group of expert e; gbase[E] = number of groups
-  int E, tmax;
-  // group g -> expert, first token, tokens
-  __device__ void info(int g, int& e, int& t0, int& T) const {
-    int lo = 0, hi = E - 1;  // largest e with gbase[e] <= g (always a non-empty expert)
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (gbase[mid] <= g) lo = mid; else hi = mid - 1;
-    }
-    e = lo;
-    const int start = lo ? end[lo - 1] : 0;
-    const int i = g - gbase[lo];
-    t0 = start + i * tmax;
-    const int rem = end[lo] - t0;
-    T = rem < tmax ? rem : tmax;
-  }
-};
-
 __device__ __forceinline__ int load_row32(const void* rows, int row_i32, int64_t t, int64_t batch) {
   const int64_t r = row_i32 ? (int64_t) static_cast<const int32_t*>(rows)[t] : static_cast<const int64_t*>(rows)[t];
   return (r >= 0 && r < batch) ? (int)r : -1;
@@ -170,8 +209,8 @@ __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uin
 // needed.  Fills s_end, chooses tmax, fills s_gbase.  Returns the group count.
 // g0 = group_list[threadIdx.x] (0 past E), loaded by the caller at kernel entry so that
 // its latency overlaps the barrier and TMEM set-up.
-__device__ int decode_groups(const GemmParams& p, int64_t g0, int32_t* s_end, int32_t* s_gbase, int64_t* scratch,
-                             uint32_t* s_err, int& tmax_out) {
+__device__ int decode_groups(const GemmParams& p, int64_t g0, int32_t* s_end, int32_t* s_gbase, int32_t* s_wbase,
+                             int64_t* scratch, uint32_t* s_err, int& tmax_out) {
   const int E = p.E;
   const int64_t M = p.M;
   const int tid = threadIdx.x;
@@ -207,18 +246,31 @@ __device__ int decode_groups(const GemmParams& p, int64_t g0, int32_t* s_end, in
   cta_scan<true, kGemmThreads>(mx, scratch, mx_all);
   int tmax = mx_all <= 32 ? 32 : (mx_all <= 64 ? 64 : 128);
   if (p.tmax_fixed) tmax = p.tmax_fixed;
-  // first group of every expert
-  int64_t gcarry = 0;
+  // first group of every expert, and (when groups can differ much in size) the cost prefix
+  // of the experts' items
+  const bool weigh = tmax >= 64;
+  int64_t gcarry = 0, wcarry = 0;
   for (int base = 0; base < E; base += kGemmThreads) {
     const int e = base + tid;
     const int64_t c = e < E ? s_end[e] - (e ? s_end[e - 1] : 0) : 0;
     const int64_t ng = (c + tmax - 1) / tmax;
-    int64_t tot;
+    const int64_t w = ng > 0 ? (ng - 1) * item_cost(tmax) + item_cost((int)(c - (ng - 1) * tmax)) : 0;
+    int64_t tot, wtot;
     const int64_t incl = cta_scan<false, kGemmThreads>(ng, scratch, tot) + gcarry;
-    if (e < E) s_gbase[e] = (int32_t)(incl - ng);
+    int64_t wincl = 0;
+    wtot = 0;
+    if (weigh) wincl = cta_scan<false, kGemmThreads>(w, scratch, wtot) + wcarry;  // uniform branch
+    if (e < E) {
+      s_gbase[e] = (int32_t)(incl - ng);
+      s_wbase[e] = (int32_t)((wincl - w) < INT32_MAX ? wincl - w : INT32_MAX);
+    }
     gcarry += tot;
+    wcarry += wtot;
   }
-  if (tid == 0) s_gbase[E] = (int32_t)gcarry;
+  if (tid == 0) {
+    s_gbase[E] = (int32_t)gcarry;
+    s_wbase[E] = weigh && wcarry < INT32_MAX ? (int32_t)wcarry : -1;  // -1: split by item count instead
+  }
   __syncthreads();
   tmax_out = tmax;
   return (int)gcarry;
@@ -307,6 +359,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* stall = drain + 1;                   // [1] never arrived on (testing aid)
   int32_t* s_end = reinterpret_cast<int32_t*>(smem + cfg::kEndOff);
   int32_t* s_gbase = reinterpret_cast<int32_t*>(smem + cfg::kGbaseOff);
+  int32_t* s_wbase = reinterpret_cast<int32_t*>(smem + cfg::kWbaseOff);
   int64_t* s_scan = reinterpret_cast<int64_t*>(smem + cfg::kScanOff);
   int32_t* misc = reinterpret_cast<int32_t*>(smem + cfg::kMiscOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&misc[0]);
@@ -338,18 +391,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   __syncthreads();
   int tmax;
-  const int n_groups = decode_groups(p, g0, s_end, s_gbase, s_scan, s_err, tmax);
+  const int n_groups = decode_groups(p, g0, s_end, s_gbase, s_wbase, s_scan, s_err, tmax);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const Groups groups{s_end, s_gbase, p.E, tmax};
+  const Groups groups{s_end, s_gbase, s_wbase, p.E, tmax};
   const int stage_bytes = cfg::stage_bytes(tmax);
   const int n_stages = cfg::n_stages(tmax);
   const Ctl ctl{abort_flag, s_err, p.timeout_ns};
   Sched sched;
-  sched.init(n_groups, p.NT, p.KB, p.deterministic != 0, p.split);
+  sched.init(n_groups, p.NT, p.KB, p.deterministic != 0, p.split, groups);
   const uint32_t smem_base = ptx::smem_u32(smem);
 
   if (warp == 0) {
