@@ -1,4 +1,5 @@
 // Auxiliary kernels of MXFP8 grouped-matmul-finalize-routing:
+//   - E2M1 (MXFP4) token expansion to E4M3,
 //   - weight preparation (one-time re-layout of x2 and its scales into GEMM tiles),
 //   - deterministic-mode routing (row CSR of the routed tokens),
 //   - deterministic combine (row-ordered sum of the per-token results).
@@ -16,32 +17,45 @@ __device__ __forceinline__ uint8_t e2m1_to_e4m3(uint32_t c) {
   return (uint8_t)(v | ((c & 8) << 4));
 }
 
+// Eight E2M1 codes (nibble i = element i) -> eight E4M3 bytes: the magnitude selects a byte
+// of the table above with a byte permute, the sign a 0x00 or 0x80 byte.
+__device__ __forceinline__ uint4 e2m1x16_to_e4m3(uint32_t a, uint32_t b) {
+  constexpr uint32_t kLo = 0x3C383000u, kHi = 0x4C484440u;
+  uint32_t o[4];
+  const uint32_t w[2] = {a, b};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t mag = w[h] & 0x77777777u;         // selectors 0..7, bit 3 clear
+    const uint32_t sgn = (w[h] >> 1) & 0x44444444u;  // selector 4 (the 0x80 byte) where the sign is set
+    o[2 * h] = __byte_perm(kLo, kHi, mag) | __byte_perm(0u, 0x80u, sgn);
+    o[2 * h + 1] = __byte_perm(kLo, kHi, mag >> 16) | __byte_perm(0u, 0x80u, sgn >> 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // packed [n_bytes] (two codes per byte, even element low) -> fp8 [2 * n_bytes]
 // n_vec: leading bytes handled 16 at a time (0 when either pointer is not 16-byte aligned)
 __global__ void __launch_bounds__(256) expand_fp4_kernel(const uint8_t* packed, uint8_t* fp8, int64_t n_bytes,
                                                          int64_t n_vec) {
   const int64_t n16 = n_vec / 16;
-  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n16; i += (int64_t)gridDim.x * 256) {
-    const uint4 in = reinterpret_cast<const uint4*>(packed)[i];
-    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    uint32_t o[8];
+  const int64_t stride = (int64_t)gridDim.x * 256;
+  const uint4* in4 = reinterpret_cast<const uint4*>(packed);
+  uint4* out4 = reinterpret_cast<uint4*>(fp8);
+  int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {  // four independent loads in flight
+    uint4 v[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t lo = 0, hi = 0;
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(in4 + i + u * stride);
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const uint32_t byte = (w[q] >> (8 * b)) & 0xFFu;
-        lo |= (uint32_t)e2m1_to_e4m3(byte & 15) << (16 * b);
-        lo |= (uint32_t)e2m1_to_e4m3(byte >> 4) << (16 * b + 8);
-        const uint32_t byte2 = (w[q] >> (8 * (b + 2))) & 0xFFu;
-        hi |= (uint32_t)e2m1_to_e4m3(byte2 & 15) << (16 * b);
-        hi |= (uint32_t)e2m1_to_e4m3(byte2 >> 4) << (16 * b + 8);
-      }
-      o[2 * q] = lo;
-      o[2 * q + 1] = hi;
+    for (int u = 0; u < 4; ++u) {
+      out4[2 * (i + u * stride)] = e2m1x16_to_e4m3(v[u].x, v[u].y);
+      out4[2 * (i + u * stride) + 1] = e2m1x16_to_e4m3(v[u].z, v[u].w);
     }
-    reinterpret_cast<uint4*>(fp8)[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
-    reinterpret_cast<uint4*>(fp8)[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  for (; i < n16; i += stride) {
+    const uint4 v = __ldg(in4 + i);
+    out4[2 * i] = e2m1x16_to_e4m3(v.x, v.y);
+    out4[2 * i + 1] = e2m1x16_to_e4m3(v.z, v.w);
   }
   for (int64_t i = n16 * 16 + (int64_t)blockIdx.x * 256 + threadIdx.x; i < n_bytes; i += (int64_t)gridDim.x * 256) {
     const uint32_t byte = packed[i];
