@@ -348,6 +348,13 @@ def test_mxfp4_raw_weights_in_call():
     assert bits == flags
 
 
+def test_deterministic_many_tokens():
+    """Deterministic mode with 9000 routed tokens over 3000 rows (row CSR of many tokens)."""
+    spec = W.Spec("det many tokens", batch=3000, M=9000, K=128, N=256, E=8, rows="random", counts="multinomial",
+                  shared_rows=100, shared_offset=7, shared_weight=0.3, out_init="randn", seed=77)
+    check_full(spec, W.make_inputs(spec), deterministic=True)
+
+
 def test_config4_deterministic_bit_stable():
     spec = W.config(4)
     inp = W.make_inputs(spec, weights_device="cuda")
