@@ -8,8 +8,8 @@ mode the row-ordered combine) on the chosen workload, weights prepared once
 beforehand (the preparation is timed separately).  `value` is the effective
 HBM bandwidth: algorithmic bytes (x2 and scales of experts holding tokens, x1,
 token scales, logit, row_index, group_list, shared_input, out read + written)
-over the device time of the call.  L2 is flushed (256 MB written) between
-steps, outside the timed events.  Multi-GPU runs are independent replicas.
+over the device time of the call.  L2 is flushed between steps (256 MB written,
+then 256 MB read), outside the timed events.  Multi-GPU runs are independent replicas.
 Prints one JSON line on rank 0.
 """
 from __future__ import annotations
@@ -62,8 +62,25 @@ def _config_dict(spec, counts, deterministic):
             "transpose_x2": spec.transpose_x2, "group_list_type": spec.group_list_type,
             "nonempty_experts": int((counts > 0).sum()), "max_tokens_per_expert": int(counts.max()),
             "mode": "deterministic" if deterministic else "atomic",
-            "l2": "flushed between steps (256 MB write), weights also larger than L2",
+            "l2": "flushed between steps (256 MB write, then 256 MB read: no inputs and no dirty lines in L2), weights also larger than L2",
             "parallelism": "replicas"}
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: writes a 256 MB buffer (twice the L2), then reads
+    another 256 MB buffer, so the next step starts with none of its inputs in L2 and
+    with no dirty lines left to write back (a write-only flush leaves ~129 MB of dirty
+    lines that the next timed kernel would pay for in HBM write-back)."""
+
+    def __init__(self):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.amax(self.r)
 
 
 class ClockSampler:
@@ -211,7 +228,7 @@ def _time_route(args, flush):
         call()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in ev:
-        flush.zero_()
+        flush()
         torch.cuda._sleep(200000)
         a.record()
         call()
@@ -239,7 +256,7 @@ def _time_ffn(args, flush):
         B.ffn(d["sorted_tokens"], prep, d["expert_cumsum"], fs.H, fs.I, fs.E, result=res, ws=ws)
     B.gmmfr_profile_begin(args.steps)
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         torch.cuda._sleep(200000)
         B.ffn(d["sorted_tokens"], prep, d["expert_cumsum"], fs.H, fs.I, fs.E, result=res, ws=ws)
     k = B.gmmfr_profile_end(args.steps)
@@ -274,7 +291,7 @@ def _time_mxfp4(args, flush):
         B.run(prob, d, out, prepared=prep, ws=ws)
     B.gmmfr_profile_begin(args.steps)
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         torch.cuda._sleep(200000)
         B.run(prob, d, out, prepared=prep, ws=ws)
     k = B.gmmfr_profile_end(args.steps)
@@ -360,7 +377,7 @@ def run_ours(args):
     ws = B.workspace(prob, True, "cuda")
     out0 = d["out"].clone()
     out = d["out"].clone()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
 
     def call(o):
         B.run(prob, d, o, prepared=prep, ws=ws)
@@ -383,7 +400,7 @@ def run_ours(args):
         with ClockSampler(local, enabled=with_clocks) as clk:
             t_wall = time.perf_counter()
             for i in range(n):
-                flush.zero_()
+                flush()
                 out.copy_(out0)
                 torch.cuda._sleep(sleep_cycles)
                 starts[i].record()
@@ -434,7 +451,7 @@ def run_ours(args):
     dd.update(dev)
     for i in range(args.warmup + args.steps):
         if i >= args.warmup:
-            flush.zero_()
+            flush()
             ee0[i - args.warmup].record()
         dev_buf.copy_(host_buf, non_blocking=True)
         B.run(prob, dd, dev["out"], prepared=prep, ws=ws)
