@@ -165,6 +165,9 @@ GMMFR_API gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int ha
  * ascending order, and results are bit-identical run to run on one device.
  * Device-side index errors do not fail the call: they set bits of the device
  * error word, read with gmmfr_check_device_errors.
+ * The grouped GEMM is launched as a programmatic dependent of the previous kernel in
+ * `stream`: when that kernel allows it (gmmfr_moe_route does), the GEMM's launch
+ * overlaps its tail; the GEMM reads no input before that kernel has completed.
  */
 GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing(
     const gmmfr_problem* problem, const void* x1, const void* x2, const void* scale,

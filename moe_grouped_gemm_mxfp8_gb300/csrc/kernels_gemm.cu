@@ -367,6 +367,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* s_err = reinterpret_cast<uint32_t*>(&misc[2]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // launched as a programmatic dependent of the kernel before it (the routing step): every
+  // input may be that kernel's output, so nothing is read before it has completed
+  ptx::griddep_wait();
   const int64_t g0 = threadIdx.x < p.E ? p.group_list[threadIdx.x] : 0;
 
   if (threadIdx.x == 0) {
@@ -639,8 +642,20 @@ cudaError_t launch_gemm(const TokenMaps& tmaps, const GemmParams& p, int grid, c
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gemm_kernel<<<grid, kGemmThreads, cfg::kSmemBytes, s>>>(tmaps, p);
-  return cudaGetLastError();
+  // programmatic stream serialization: the launch (and block scheduling) may overlap the tail
+  // of the previous kernel in the stream when that kernel allows it; the kernel waits for it
+  // before reading any input
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid);
+  lc.blockDim = dim3(kGemmThreads);
+  lc.dynamicSmemBytes = cfg::kSmemBytes;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, gemm_kernel, tmaps, p);
 }
 
 }  // namespace gmmfr

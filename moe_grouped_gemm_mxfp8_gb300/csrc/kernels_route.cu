@@ -20,6 +20,7 @@
 #include <cstdlib>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace gmmfr {
 
@@ -162,6 +163,7 @@ __device__ __forceinline__ void scatter_entry(const RouteScatterParams& p, int64
 }
 
 __global__ void __launch_bounds__(256) route_scatter_kernel(RouteScatterParams p) {
+  ptx::griddep_launch_dependents();  // the operator that follows may start launching (it waits for us)
   const int lane = threadIdx.x & 31;
   const int64_t f = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (f >= p.M) return;
@@ -178,6 +180,7 @@ __global__ void __launch_bounds__(kFuseThreads, 4) route_fused_kernel(RouteScatt
   __shared__ int32_t s_pos[kFuseMaxSlice];
   __shared__ int32_t s_wsum[kFuseThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  ptx::griddep_launch_dependents();  // the operator that follows may start launching (it waits for us)
   const int keys = p.E + 1;
   const int M = (int)p.M;
   const int f_lo = (int)((int64_t)M * blockIdx.x / gridDim.x);
