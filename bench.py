@@ -28,6 +28,9 @@ sys.path.insert(0, ROOT)
 METRIC = "µs/call and achieved HBM GB/s vs roofline, MXFP8 grouped-matmul-finalize-routing"
 DEFAULT_CONFIG = 2
 FMT_NAMES = {0: "E4M3", 1: "E5M2", 2: "E2M1"}
+# GPU sleep placed before each timed call, outside its events (about 0.5 ms at 2 GHz): the
+# device stays busy while the host enqueues the call, so the events time device work only
+SLEEP_CYCLES = 1_000_000
 
 
 def reduce_step_time(ms: float, world: int) -> float:
@@ -229,7 +232,7 @@ def _time_route(args, flush):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in ev:
         flush()
-        torch.cuda._sleep(200000)
+        torch.cuda._sleep(SLEEP_CYCLES)
         a.record()
         call()
         b.record()
@@ -270,7 +273,7 @@ def _time_layer(args, flush, prob, d, prep, ws, call_us, route_us):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in ev:
         flush()
-        torch.cuda._sleep(200000)
+        torch.cuda._sleep(SLEEP_CYCLES)
         a.record()
         layer()
         b.record()
@@ -303,7 +306,7 @@ def _time_ffn(args, flush):
     B.gmmfr_profile_begin(args.steps)
     for _ in range(args.steps):
         flush()
-        torch.cuda._sleep(200000)
+        torch.cuda._sleep(SLEEP_CYCLES)
         B.ffn(d["sorted_tokens"], prep, d["expert_cumsum"], fs.H, fs.I, fs.E, result=res, ws=ws)
     k = B.gmmfr_profile_end(args.steps)
     ms = statistics.mean(x[4] for x in k)
@@ -338,7 +341,7 @@ def _time_mxfp4(args, flush):
     B.gmmfr_profile_begin(args.steps)
     for _ in range(args.steps):
         flush()
-        torch.cuda._sleep(200000)
+        torch.cuda._sleep(SLEEP_CYCLES)
         B.run(prob, d, out, prepared=prep, ws=ws)
     k = B.gmmfr_profile_end(args.steps)
     bits = B.gmmfr_check_device_errors(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
@@ -433,7 +436,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     bits = B.gmmfr_check_device_errors(ws.data_ptr(), sptr)
 
-    sleep_cycles = 200000  # about 0.1 ms at 2 GHz
+    sleep_cycles = SLEEP_CYCLES
 
     def timed_steps(n, with_clocks):
         """n steps of: L2 flush, reset of out, a GPU sleep (so the host has enqueued the
