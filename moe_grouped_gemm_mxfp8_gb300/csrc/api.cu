@@ -587,6 +587,7 @@ gmmfr_status gmmfr_llada2_moe_grouped_gemm(const gmmfr_ffn_problem* problem, con
   fp.KB = (int32_t)kb2;
   fp.gate_up = 0;
   fp.slot_base = grid;
+  fp.dependent = 1;
   timer.begin(3, s);
   e = gmmfr::launch_ffn_gemm(m2, fp, grid, s);
   timer.end(3, s);

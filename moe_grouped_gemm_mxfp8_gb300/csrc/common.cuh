@@ -129,6 +129,8 @@ struct FfnParams {
   int32_t E, NT, KB;
   int32_t gate_up;          // 1: SwiGLU epilogue
   int32_t slot_base;        // first error slot of this launch
+  int32_t dependent;        // launched as a programmatic dependent of GEMM1: sw is read only after
+                            // griddepcontrol.wait (weight tiles stream before it)
   uint32_t idesc;
   int64_t timeout_ns;
 };

@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
   int* abort_flag = &misc[1];
   uint32_t* s_err = reinterpret_cast<uint32_t*>(&misc[2]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (p.gate_up) ptx::griddep_launch_dependents();  // GEMM2 may launch (it waits for GEMM1 before reading sw)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ffn::kMaxStages; ++s) {
@@ -257,6 +258,36 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // GEMM2 launched as a dependent of GEMM1: the weight tiles do not depend on GEMM1, so
+      // the first ring's worth is requested before waiting for GEMM1 (the token rows, its
+      // output, only after); those stages are remembered in `pend`
+      bool waited = !p.dependent;
+      int np = 0;
+      int pend_stage[ffn::kMaxStages], pend_kb[ffn::kMaxStages], pend_t0[ffn::kMaxStages], pend_m[ffn::kMaxStages];
+      auto token_rows = [&](uint32_t sb, uint32_t fb, int kb, int t0, int m) {
+        int row = 0;  // a 128-row box, or a 64-row box, then 32-row boxes and a last 16-row box
+        if (m == 8) {
+          ptx::tma_load_2d(sb + ffn::kOffX, &tmaps.m[3], kb * 64, t0, fb, pol_keep);
+          row = 128;
+        } else if (m > 4) {
+          ptx::tma_load_2d(sb + ffn::kOffX, &tmaps.m[2], kb * 64, t0, fb, pol_keep);
+          row = 64;
+        }
+        for (; row < m * 16; row += 32) {
+          const int last16 = row + 16 == m * 16;
+          ptx::tma_load_2d(sb + ffn::kOffX + row * 128, &tmaps.m[last16 ? 0 : 1], kb * 64, t0 + row, fb, pol_keep);
+        }
+      };
+      auto release_pending = [&]() {
+        ptx::griddep_wait();
+        for (int i = 0; i < np; ++i) {
+          const uint32_t fb = ptx::smem_u32(&full[pend_stage[i]]);
+          ptx::mbar_arrive_expect_tx(fb, pend_m[i] * 16 * 128);
+          token_rows(smem_base + pend_stage[i] * stage_bytes, fb, pend_kb[i], pend_t0[i], pend_m[i]);
+        }
+        np = 0;
+        waited = true;
+      };
       for (int64_t u = u_begin; ok && u < u_end; ++u) {
         const int g = (int)(u / p.NT), j = (int)(u % p.NT);
         int e, t0, T;
@@ -272,25 +303,33 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
           }
           const uint32_t fb = ptx::smem_u32(&full[stage]);
           const uint32_t sb = smem_base + stage * stage_bytes;
-          ptx::mbar_arrive_expect_tx(fb, tx);
-          ptx::bulk_g2s(sb, wsrc + (int64_t)kb * kWTileBytes, kWTileBytes, fb, pol_w);
-          int row = 0;  // token rows: a 128-row box, or a 64-row box, then 32-row boxes and a last 16-row box
-          if (m == 8) {
-            ptx::tma_load_2d(sb + ffn::kOffX, &tmaps.m[3], kb * 64, t0, fb, pol_keep);
-            row = 128;
-          } else if (m > 4) {
-            ptx::tma_load_2d(sb + ffn::kOffX, &tmaps.m[2], kb * 64, t0, fb, pol_keep);
-            row = 64;
-          }
-          for (; row < m * 16; row += 32) {
-            const int last16 = row + 16 == m * 16;
-            ptx::tma_load_2d(sb + ffn::kOffX + row * 128, &tmaps.m[last16 ? 0 : 1], kb * 64, t0 + row, fb, pol_keep);
+          if (waited) {
+            ptx::mbar_arrive_expect_tx(fb, tx);
+            ptx::bulk_g2s(sb, wsrc + (int64_t)kb * kWTileBytes, kWTileBytes, fb, pol_w);
+            token_rows(sb, fb, kb, t0, m);
+          } else {  // weights now; the arrival with the token rows after GEMM1
+            ptx::mbar_expect_tx(fb, kWTileBytes);
+            ptx::bulk_g2s(sb, wsrc + (int64_t)kb * kWTileBytes, kWTileBytes, fb, pol_w);
+            pend_stage[np] = stage;
+            pend_kb[np] = kb;
+            pend_t0[np] = t0;
+            pend_m[np] = m;
+            if (++np == n_stages) release_pending();  // every stage is in use: the ring needs the tokens
           }
           ++fills[stage];
           if (++stage == n_stages) {
             stage = 0;
             phase ^= 1;
           }
+        }
+      }
+      if (!waited) {
+        if (ok) {
+          release_pending();  // fewer items than stages
+        } else {            // aborted: complete the pending phases without tokens so they can drain
+          for (int i = 0; i < np; ++i) ptx::mbar_arrive(ptx::smem_u32(&full[pend_stage[i]]));
+          np = 0;
+          ptx::griddep_wait();
         }
       }
       if (ok) {
@@ -423,8 +462,21 @@ cudaError_t launch_ffn_gemm(const TokenMaps& tmaps, const FfnParams& p, int grid
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  ffn_gemm_kernel<<<grid, ffn::kThreads, ffn::kSmemBytes, s>>>(tmaps, p);
-  return cudaGetLastError();
+  if (!p.dependent) {
+    ffn_gemm_kernel<<<grid, ffn::kThreads, ffn::kSmemBytes, s>>>(tmaps, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t lc = {};  // programmatic dependent of the previous kernel (GEMM1)
+  lc.gridDim = dim3((unsigned)grid);
+  lc.blockDim = dim3(ffn::kThreads);
+  lc.dynamicSmemBytes = ffn::kSmemBytes;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, ffn_gemm_kernel, tmaps, p);
 }
 
 }  // namespace gmmfr
