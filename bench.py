@@ -33,6 +33,12 @@ FMT_NAMES = {0: "E4M3", 1: "E5M2", 2: "E2M1"}
 SLEEP_CYCLES = 1_000_000
 
 
+def _quantiles(xs, qs):
+    """Nearest-rank quantiles of a list."""
+    v = sorted(xs)
+    return [v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))] for q in qs]
+
+
 def reduce_step_time(ms: float, world: int) -> float:
     """Slowest rank's mean step time (the job's step time).  Replicas share no
     data: the only cross-rank operation is this max."""
@@ -541,6 +547,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "mxfp8 (fp8 x fp8, e8m0 per 32) -> f32", "data": "synthetic",
         "config": _config_dict(spec, counts, args.deterministic),
         "us_per_call": ms * 1e3, "us_per_call_min": min(call_ms) * 1e3,
+        "us_per_call_p10_p50_p90": [round(float(x) * 1e3, 2) for x in _quantiles(call_ms, (0.1, 0.5, 0.9))],
         "us_per_call_profiled": statistics.mean(k[4] for k in kernel_ms) * 1e3, "tflops": flops / (ms * 1e-3) / 1e12,
         "roofline_fraction_call": gbs / world / hbm_peak,
         "kernels_ms": {"route": pro_ms, "gemm": gemm_ms, "combine": comb_ms},
@@ -575,8 +582,8 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
