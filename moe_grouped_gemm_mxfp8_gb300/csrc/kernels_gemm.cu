@@ -134,7 +134,7 @@ struct Sched {
   int64_t i, i_end, step;
   int NT, KB, split, ng;
   bool det;
-  bool small;  // the whole iteration space fits 31 bits: 32-bit index arithmetic
+  int cur_g, cur_j, cur_kb;  // atomic mode: group, column tile and K block of item i
   __device__ void init(int n_groups, int NT_, int KB_, bool det_, int split_, const Groups& gr) {
     ng = n_groups;
     NT = NT_;
@@ -142,54 +142,57 @@ struct Sched {
     det = det_;
     split = split_;
     const int64_t tiles = (int64_t)n_groups * NT;
-    if (!det && gr.wbase[gr.E] > 0) {
+    if (det) {
+      i = blockIdx.x;
+      i_end = tiles * split;
+      step = gridDim.x;
+      return;
+    }
+    step = 0;
+    if (gr.wbase[gr.E] > 0) {
       // equal cost per CTA: items of large token groups move more bytes than those of small ones
       const int64_t total = (int64_t)NT * KB * gr.wbase[gr.E];
       i = gr.item_at(total * blockIdx.x / gridDim.x, KB, NT, n_groups);
       i_end = gr.item_at(total * (blockIdx.x + 1) / gridDim.x, KB, NT, n_groups);
-      step = 0;
-    } else if (!det) {
-      const int64_t total = tiles * KB;
-      i = total * blockIdx.x / gridDim.x;
-      i_end = total * (blockIdx.x + 1) / gridDim.x;
-      step = 0;
     } else {
-      i = blockIdx.x;
-      i_end = tiles * split;
-      step = gridDim.x;
+      const int64_t total = tiles * KB;
+      if (total * gridDim.x < ((int64_t)1 << 32)) {  // 32-bit division where it fits
+        i = (uint32_t)(total * blockIdx.x) / gridDim.x;
+        i_end = (uint32_t)(total * (blockIdx.x + 1)) / gridDim.x;
+      } else {
+        i = total * blockIdx.x / gridDim.x;
+        i_end = total * (blockIdx.x + 1) / gridDim.x;
+      }
     }
-    small = i_end + step < ((int64_t)1 << 31);
+    // position of the first item; next() then walks tiles without dividing
+    const int64_t tile = i / KB;
+    cur_kb = (int)(i - tile * KB);
+    cur_g = (int)(tile % (ng > 0 ? ng : 1));
+    cur_j = (int)(tile / (ng > 0 ? ng : 1));
   }
   __device__ bool next(Seg& s) {
     if (i >= i_end) return false;
-    if (small && !det) {  // the common case, without 64-bit divisions
-      const uint32_t i32 = (uint32_t)i, kb = (uint32_t)KB;
-      const uint32_t tile = i32 / kb;
-      s.kb0 = (int)(i32 - tile * kb);
-      const uint32_t left = (uint32_t)(i_end - i);
-      s.kb1 = (kb - s.kb0) < left ? (int)kb : s.kb0 + (int)left;
-      i += s.kb1 - s.kb0;
+    if (!det) {  // tiles in order j * n_groups + g; a segment runs to its tile's end or the range's
+      s.g = cur_g;
+      s.j = cur_j;
+      s.kb0 = cur_kb;
+      const int64_t left = i_end - i;
+      s.kb1 = (KB - cur_kb) < left ? KB : cur_kb + (int)left;
       s.slot = 0;
-      s.g = (int)(tile % (uint32_t)ng);
-      s.j = (int)(tile / (uint32_t)ng);
+      i += s.kb1 - s.kb0;
+      cur_kb = 0;
+      if (++cur_g == ng) {
+        cur_g = 0;
+        ++cur_j;
+      }
       return true;
     }
-    int64_t tile;
-    if (!det) {
-      tile = i / KB;
-      s.kb0 = (int)(i % KB);
-      const int64_t left = i_end - i;
-      s.kb1 = (int)((KB - s.kb0) < left ? KB : s.kb0 + left);
-      i += s.kb1 - s.kb0;
-      s.slot = 0;
-    } else {
-      tile = i / split;
-      const int sp = (int)(i % split);
-      s.kb0 = (int)((int64_t)sp * KB / split);
-      s.kb1 = (int)((int64_t)(sp + 1) * KB / split);
-      s.slot = sp;
-      i += step;
-    }
+    const int64_t tile = i / split;
+    const int sp = (int)(i % split);
+    s.kb0 = (int)((int64_t)sp * KB / split);
+    s.kb1 = (int)((int64_t)(sp + 1) * KB / split);
+    s.slot = sp;
+    i += step;
     s.g = (int)(tile % ng);
     s.j = (int)(tile / ng);
     return true;
