@@ -108,11 +108,19 @@ struct FfnGroups {
   const int32_t* end;
   const int32_t* gbase;
   int E, tmax, start0;
+  // e is also a hint (the expert of an earlier group of the range, or -1): walk forward from it
   __device__ void info(int g, int& e, int& t0, int& T) const {
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (gbase[mid] <= g) lo = mid; else hi = mid - 1;
+    int lo;
+    if (e >= 0 && gbase[e] <= g) {
+      lo = e;
+      while (gbase[lo + 1] <= g) ++lo;
+    } else {
+      lo = 0;
+      int hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (gbase[mid] <= g) lo = mid; else hi = mid - 1;
+      }
     }
     e = lo;
     const int start = lo ? end[lo - 1] : start0;
@@ -245,6 +253,9 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
   // streams consecutive prepared tiles of one expert and re-reads that expert's token rows
   const int64_t n_units = (int64_t)n_groups * p.NT;
   const int64_t u_begin = n_units * blockIdx.x / gridDim.x, u_end = n_units * (blockIdx.x + 1) / gridDim.x;
+  // (group, column tile) of the first unit; every role then steps the column tile, wrapping
+  // into the next group, without dividing
+  const int g_begin = (int)(u_begin / p.NT), j_begin = (int)(u_begin % p.NT);
   const uint32_t smem_base = ptx::smem_u32(smem);
 
   if (warp == 0) {
@@ -288,10 +299,10 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
         np = 0;
         waited = true;
       };
-      for (int64_t u = u_begin; ok && u < u_end; ++u) {
-        const int g = (int)(u / p.NT), j = (int)(u % p.NT);
-        int e, t0, T;
-        groups.info(g, e, t0, T);
+      int e = -1;
+      for (int64_t u = u_begin, g = g_begin, j = j_begin; ok && u < u_end; ++u, j = (j + 1 == p.NT ? (++g, 0) : j + 1)) {
+        int t0, T;
+        groups.info((int)g, e, t0, T);
         const int m = (T + 15) / 16;
         const uint32_t tx = kWTileBytes + m * 16 * 128;
         const uint8_t* wsrc = p.prepared + ((int64_t)e * p.NT + j) * p.KB * (int64_t)kWTileBytes;
@@ -349,10 +360,10 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
       uint32_t phase = 0;
       int acc_i = 0;
       bool ok = true;
-      for (int64_t u = u_begin; ok && u < u_end; ++u) {
-        const int g = (int)(u / p.NT);
-        int e, t0, T;
-        groups.info(g, e, t0, T);
+      int e = -1;
+      for (int64_t u = u_begin, g = g_begin, j = j_begin; ok && u < u_end; ++u, j = (j + 1 == p.NT ? (++g, 0) : j + 1)) {
+        int t0, T;
+        groups.info((int)g, e, t0, T);
         const uint32_t npad = (uint32_t)((T + 15) / 16) * 16;
         const uint32_t idesc = p.idesc | ((npad >> 3) << 17);
         const int buf = acc_i & 1;
@@ -390,10 +401,10 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     int acc_i = 0;
-    for (int64_t u = u_begin; u < u_end; ++u) {
-      const int g = (int)(u / p.NT), j = (int)(u % p.NT);
-      int e, t0, T;
-      groups.info(g, e, t0, T);
+    int e = -1;
+    for (int64_t u = u_begin, g = g_begin, j = j_begin; u < u_end; ++u, j = (j + 1 == p.NT ? (++g, 0) : j + 1)) {
+      int t0, T;
+      groups.info((int)g, e, t0, T);
       const int buf = acc_i & 1;
       const bool ok = wait_bar(ptx::smem_u32(&accf[buf]), (acc_i >> 1) & 1, ctl);
       if (!epi_all(ok)) break;  // the 4 warps leave together: they share a named barrier

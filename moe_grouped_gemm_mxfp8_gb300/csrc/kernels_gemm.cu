@@ -88,12 +88,21 @@ struct Groups {
   const int32_t* wbase;  // cost of the items of experts before e in one K block of one tile
                          // (item_cost units); wbase[E] = total, < 0 when it would overflow
   int E, tmax;
-  // group g -> expert, first token, tokens
+  // group g -> expert, first token, tokens.  e is also a hint: the expert of an earlier
+  // group of the same range (or -1); the walk forward from it replaces the binary search
+  // when g has not wrapped below it.
   __device__ void info(int g, int& e, int& t0, int& T) const {
-    int lo = 0, hi = E - 1;  // largest e with gbase[e] <= g (always a non-empty expert)
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (gbase[mid] <= g) lo = mid; else hi = mid - 1;
+    int lo;  // largest e with gbase[e] <= g (always a non-empty expert)
+    if (e >= 0 && gbase[e] <= g) {
+      lo = e;
+      while (gbase[lo + 1] <= g) ++lo;
+    } else {
+      lo = 0;
+      int hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (gbase[mid] <= g) lo = mid; else hi = mid - 1;
+      }
     }
     e = lo;
     const int start = lo ? end[lo - 1] : 0;
@@ -320,14 +329,14 @@ __device__ __forceinline__ uint32_t token_scale_word(const GemmParams& p, int64_
 struct PackIter {
   Seg sg;
   int kb, kb1, t0, T;
+  int e;  // expert of the current segment (hint for the next lookup)
   bool valid;
 };
 
 __device__ __forceinline__ bool pack_next(PackIter& it, Sched& sched, const Groups& groups) {
   if (it.valid && ++it.kb < it.kb1) return true;
   while (sched.next(it.sg)) {
-    int e;
-    groups.info(it.sg.g, e, it.t0, it.T);
+    groups.info(it.sg.g, it.e, it.t0, it.T);
     it.kb = it.sg.kb0;
     it.kb1 = it.sg.kb1;
     if (it.kb < it.kb1) {
@@ -425,8 +434,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       if (p.test_stall) ok = wait_bar(ptx::smem_u32(stall), 0, ctl);
       Seg sg;
+      int e = -1;
       while (ok && sched.next(sg)) {
-        int e, t0, T;
+        int t0, T;
         groups.info(sg.g, e, t0, T);
         const int m = (T + 15) / 16;  // token rows in 16-row units: boxes of 128/64/32/16 rows
         const uint32_t tx = kPrepTileBytes + m * 16 * 128;
@@ -482,8 +492,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc_i = 0;
       Seg sg;
       bool ok = true;
+      int e = -1;
       while (ok && sched.next(sg)) {
-        int e, t0, T;
+        int t0, T;
         groups.info(sg.g, e, t0, T);
         const uint32_t npad = (uint32_t)((T + 15) / 16) * 16;
         const uint32_t idesc = p.idesc | ((npad >> 3) << 17);
@@ -532,6 +543,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // the ring.
     PackIter it;
     it.valid = false;
+    it.e = -1;
     uint32_t w0[4], w1[4], w2[4];
     bool v0 = pack_next(it, sched, groups);
     pack_load(p, it, w0);
@@ -571,8 +583,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc_i = 0;
     Seg sg;
     bool bad_row = false;
+    int e = -1;
     while (sched.next(sg)) {
-      int e, t0, T;
+      int t0, T;
       groups.info(sg.g, e, t0, T);
       const int buf = acc_i & 1;
       const uint32_t aph = (acc_i >> 1) & 1;
