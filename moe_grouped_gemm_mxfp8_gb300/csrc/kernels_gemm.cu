@@ -579,7 +579,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int ep_tid = threadIdx.x - 64;
-    if (!p.deterministic && p.shared != nullptr && p.shared_rows > 0 && p.N > 0) shared_add_slice(p, ep_tid);
+    // the shared add (atomic mode) runs after the first tile's epilogue, in time the epilogue
+    // warps spend waiting anyway; at kernel entry its atomics delayed the first weight loads
+    bool shared_pending = !p.deterministic && p.shared != nullptr && p.shared_rows > 0 && p.N > 0;
     int acc_i = 0;
     Seg sg;
     bool bad_row = false;
@@ -631,7 +633,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       ++acc_i;
+      if (shared_pending) {
+        shared_add_slice(p, ep_tid);
+        shared_pending = false;
+      }
     }
+    if (shared_pending) shared_add_slice(p, ep_tid);  // no tile, or the loop left early
     if (bad_row) atomicOr(s_err, kErrBadRowIndex);
   }
 
