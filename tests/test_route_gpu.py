@@ -104,3 +104,37 @@ def test_route_then_operator(det):
     bound = oracle.tolerance(ref, absb, init, sh)
     assert flags == 0
     assert np.all(np.abs(got - ref) <= bound)
+
+
+def test_operator_launched_right_after_routing():
+    """The operator's GEMM is a programmatic dependent of the routing kernel (its launch
+    overlaps the routing tail; it reads nothing before routing completes).  Weights are
+    prepared first, so each operator call directly follows a routing call on the stream;
+    three rounds with fresh routings, each checked against the oracles."""
+    batch, topk, K, N, E = 128, 2, 1024, 512, 16
+    gspec = W.Spec("w", batch=batch, M=batch * topk, K=K, N=N, E=E, seed=41, shared_rows=batch, out_init="randn")
+    gi = W.make_inputs(gspec)
+    prob = B.problem_from_spec(gspec)
+    prep = B.prepare_weights(prob, gi["x2"].cuda(), gi["scale"].cuda())
+    shared = gi["shared_input"].cuda()
+    torch.cuda.synchronize()
+    for rnd in range(3):
+        rs = W.RouteSpec("t", batch=batch, topk=topk, K=K, E=E, seed=50 + rnd)
+        ri = W.make_route_inputs(rs)
+        dev = {k: v.cuda() for k, v in ri.items()}
+        res = gi["out"].cuda().clone()
+        torch.cuda.synchronize()
+        out, _ = B.route(dev["topk_ids"], dev["topk_weights"], dev["x"], dev["x_scale"], E)
+        d = dict(x1=out["x1"], pertoken_scale=out["pertoken_scale"], group_list=out["group_list"],
+                 logit=out["logit"], row_index=out["row_index"], shared_input=shared)
+        B.run(prob, d, res, prepared=prep)
+        got = res.cpu().numpy().astype(np.float64)
+        r = R.moe_route(ri["topk_ids"].numpy(), ri["topk_weights"].numpy(), ri["x"].numpy(), ri["x_scale"].numpy(), E)
+        p = oracle.Problem(M=batch * topk, K=K, N=N, E=E, batch=batch, x1=r["x1"], x2=gi["x2"], scale=gi["scale"],
+                           pertoken_scale=r["pertoken_scale"], group_list=r["group_list"], row_index=r["row_index"],
+                           out=gi["out"], logit=r["logit"], shared_input=gi["shared_input"])
+        ref, absb, flags = oracle.run(p)
+        bound = oracle.tolerance(ref, absb, gi["out"].numpy().astype(np.float64),
+                                 gi["shared_input"].to(torch.float64).numpy())
+        assert flags == 0
+        assert np.all(np.abs(got - ref) <= bound), rnd
