@@ -53,9 +53,11 @@ typedef enum {
  * MXFP4 scenario (aclnn V3, Atlas 350) stored two codes per byte along the row's
  * contiguous dimension (K for x1 and a transposed x2, N for a non-transposed x2),
  * the even element in the low nibble; K, and N for a non-transposed E2M1 x2, even
- * (aclnn: "k must be even; n even when x2 is not transposed").  E2M1 operands are
- * expanded exactly to E4M3 (weights at preparation, tokens per call) and run on the
- * FP8 block-scaled MMA. */
+ * (aclnn: "k must be even; n even when x2 is not transposed").  When x1 and x2 are
+ * both E2M1 and K % 32 == 0 they stay packed and run on the FP4 block-scaled MMA
+ * (kind::mxf4, 256 K elements per tile).  Otherwise an E2M1 operand is expanded exactly
+ * to E4M3 (weights at preparation, tokens per call) and runs on the FP8 block-scaled MMA
+ * beside the other operand's FP8 codes. */
 typedef enum { GMMFR_E4M3 = 0, GMMFR_E5M2 = 1, GMMFR_E2M1 = 2 } gmmfr_fp8_format;
 
 /* Integer type of row_index: int64 as in the tensor table, or int32. */
@@ -111,7 +113,8 @@ typedef struct {
 
 /*
  * Bytes of the prepared-weight buffer for this problem's x2 and scale
- * (E x ceil(N/128) x ceil(K/128) tiles of 16896 bytes).  Host only; no CUDA call.
+ * (E x ceil(N/128) x ceil(K/128) tiles of 16896 bytes; packed E2M1 x1 and x2 with
+ * K % 32 == 0: E x ceil(N/128) x ceil(K/256) tiles of 17408 bytes).  Host only; no CUDA call.
  * Returns GMMFR_ERR_INVALID_ARG on an invalid problem.
  */
 GMMFR_API gmmfr_status gmmfr_prepared_weights_size(const gmmfr_problem* problem, size_t* bytes);
@@ -122,7 +125,10 @@ GMMFR_API gmmfr_status gmmfr_prepared_weights_size(const gmmfr_problem* problem,
  * weights followed by its 512 scale bytes), so that each tile is a single
  * contiguous HBM read.  Inputs as in section 3.1 (x2 [E,K,N] or [E,N,K]; scale
  * [(E,)ceil(K/64),N,2] or [(E,)N,ceil(K/64),2]); an E2M1 x2 is packed two codes
- * per byte along its last dimension and is stored prepared as E4M3 codes.
+ * per byte along its last dimension.  With E2M1 tokens too (and K % 32 == 0) a tile
+ * keeps the codes packed: 128 columns x 256 K (K pairs per byte, the lower K in the low
+ * nibble) and then 1024 scale bytes (eight per row, in two 512-byte halves); otherwise
+ * the E2M1 codes are stored prepared as E4M3 codes.
  *   prepared        device buffer of at least gmmfr_prepared_weights_size bytes,
  *                   16-byte aligned, caller-owned; fully overwritten.
  * Enqueued on `stream`; the buffer stays valid as long as the caller keeps it.
@@ -133,8 +139,8 @@ GMMFR_API gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const
 /*
  * Workspace bytes one call needs (two-phase use as in aclnn's
  * GetWorkspaceSize/execute pair).  `have_prepared` = 0 adds room to prepare
- * the weights inside the call; an E2M1 x1 adds M*K bytes for its expansion to
- * E4M3.  Host only; may query the current device's SM count.  The workspace
+ * the weights inside the call; an E2M1 x1 that is expanded (x2 not E2M1, or
+ * K % 32 != 0) adds M*K bytes for its expansion to E4M3.  Host only; may query the current device's SM count.  The workspace
  * must be 256-byte aligned.
  */
 GMMFR_API gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int have_prepared, size_t* bytes);

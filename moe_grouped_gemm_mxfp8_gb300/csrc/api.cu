@@ -65,6 +65,18 @@ gmmfr_status validate(const gmmfr_problem* p) {
   return GMMFR_OK;
 }
 
+// Packed E2M1 tokens and weights stay packed (kind::mxf4, 256 K elements per 128-byte tile
+// row) when x1 rows are whole 16-byte units (K % 32 == 0, a TMA stride rule); otherwise, and
+// for mixed formats, E2M1 operands are expanded exactly to E4M3.
+bool native_fp4(const gmmfr_problem* p) {
+  return p->x1_format == GMMFR_E2M1 && p->x2_format == GMMFR_E2M1 && p->K % 32 == 0;
+}
+int64_t k_blocks(const gmmfr_problem* p) { return cdiv(p->K, native_fp4(p) ? gmmfr::kTileK4 : gmmfr::kTileK); }
+size_t prepared_bytes(const gmmfr_problem* p) {
+  return (size_t)p->E * cdiv(p->N, gmmfr::kTileN) * k_blocks(p) *
+         (native_fp4(p) ? gmmfr::kPrepTileBytes4 : gmmfr::kPrepTileBytes);
+}
+
 int device_sms() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return kSplitRefSms;
@@ -91,7 +103,7 @@ struct Layout {
 Layout make_layout(const gmmfr_problem* p, bool have_prepared) {
   Layout L{};
   L.NT = cdiv(p->N, gmmfr::kTileN);
-  L.KB = cdiv(p->K, gmmfr::kTileK);
+  L.KB = k_blocks(p);
   L.Ks = cdiv(p->K, 64);
   const bool det = p->flags & GMMFR_DETERMINISTIC;
   if (det) {
@@ -115,9 +127,9 @@ Layout make_layout(const gmmfr_problem* p, bool have_prepared) {
   }
   if (!have_prepared) {
     L.off_prep = off;
-    off = align256(off + (size_t)p->E * L.NT * L.KB * gmmfr::kPrepTileBytes);
+    off = align256(off + prepared_bytes(p));
   }
-  if (p->x1_format == GMMFR_E2M1) {  // E2M1 tokens expanded to E4M3 codes, [M, K] bytes
+  if (p->x1_format == GMMFR_E2M1 && !native_fp4(p)) {  // E2M1 tokens expanded to E4M3 codes, [M, K] bytes
     L.off_tok = off;
     off = align256(off + (size_t)p->M * p->K);
   }
@@ -180,7 +192,7 @@ const char* gmmfr_last_error(void) { return g_last_error.c_str(); }
 gmmfr_status gmmfr_prepared_weights_size(const gmmfr_problem* problem, size_t* bytes) {
   if (gmmfr_status st = validate(problem)) return st;
   if (!bytes) return fail(GMMFR_ERR_INVALID_ARG, "bytes is NULL");
-  *bytes = (size_t)problem->E * cdiv(problem->N, gmmfr::kTileN) * cdiv(problem->K, gmmfr::kTileK) * gmmfr::kPrepTileBytes;
+  *bytes = prepared_bytes(problem);
   return GMMFR_OK;
 }
 
@@ -200,11 +212,12 @@ static gmmfr::PrepParams prep_params(const gmmfr_problem* p, const void* x2, con
   pp.K = p->K;
   pp.N = p->N;
   pp.NT = (int32_t)cdiv(p->N, gmmfr::kTileN);
-  pp.KB = (int32_t)cdiv(p->K, gmmfr::kTileK);
+  pp.KB = (int32_t)k_blocks(p);
   pp.Ks = (int32_t)cdiv(p->K, 64);
   pp.transpose_x2 = p->transpose_x2;
   pp.scale_per_expert = p->scale_per_expert;
   pp.fp4 = p->x2_format == GMMFR_E2M1;
+  pp.fp4_native = native_fp4(p);
   return pp;
 }
 
@@ -262,7 +275,8 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
 
   const uint8_t* wprep = static_cast<const uint8_t*>(prepared);
   timer.begin(4, s);
-  const bool fp4_tokens = p.x1_format == GMMFR_E2M1 && p.M > 0;
+  const bool fp4 = native_fp4(problem);
+  const bool fp4_tokens = p.x1_format == GMMFR_E2M1 && !fp4 && p.M > 0;
   if (!prepared || fp4_tokens) timer.begin(0, s);
   if (!prepared) {
     e = gmmfr::launch_prep(prep_params(problem, x2, scale, ws + L.off_prep), s);
@@ -276,12 +290,14 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   }
   if (!prepared || fp4_tokens) timer.end(0, s);
 
-  // x1 [M, K] bytes as 2-D tensors of 128-byte rows: boxes of 16, 32, 64, 128 rows, 128-byte swizzle
+  // x1 [M, K] bytes (packed E2M1: [M, K/2]) as 2-D tensors of 128-byte rows: boxes of 16, 32,
+  // 64, 128 rows, 128-byte swizzle
   gmmfr::TokenMaps tmaps;
   {
     const bool empty = p.M == 0;
-    cuuint64_t dims[2] = {(cuuint64_t)(empty ? 16 : p.K), (cuuint64_t)(empty ? 1 : p.M)};
-    cuuint64_t strides[1] = {(cuuint64_t)(empty ? 16 : p.K)};
+    const int64_t row_bytes = fp4 ? p.K / 2 : p.K;
+    cuuint64_t dims[2] = {(cuuint64_t)(empty ? 16 : row_bytes), (cuuint64_t)(empty ? 1 : p.M)};
+    cuuint64_t strides[1] = {(cuuint64_t)(empty ? 16 : row_bytes)};
     cuuint32_t estr[2] = {1, 1};
     for (int b = 0; b < 4; ++b) {
       cuuint32_t box[2] = {(cuuint32_t)gmmfr::kTileK, (cuuint32_t)(gmmfr::kTokBox << b)};
@@ -340,12 +356,15 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   if (!gp.tmax_fixed && p.expected_tokens_per_expert > 0)
     gp.tmax_fixed = p.expected_tokens_per_expert <= 32 ? 32 : (p.expected_tokens_per_expert <= 64 ? 64 : 128);
   gp.split = L.split;
+  gp.fp4 = fp4;
   gp.deterministic = det;
   gp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;
   // instruction descriptor: A = weights (x2 format), B = tokens (x1 format),
-  // E8M0 scales (bit 23), M = 128 (bits 24..28 hold M >> 4); E2M1 operands arrive expanded to E4M3
-  const uint32_t afmt = p.x2_format == GMMFR_E2M1 ? GMMFR_E4M3 : (uint32_t)p.x2_format;
-  const uint32_t bfmt = p.x1_format == GMMFR_E2M1 ? GMMFR_E4M3 : (uint32_t)p.x1_format;
+  // E8M0 scales (bit 23), M = 128 (bits 24..28 hold M >> 4).  kind::mxf8f6f4 codes E4M3 0 and
+  // E5M2 1, E2M1 operands of a mixed pair arriving expanded to E4M3; kind::mxf4 has the one
+  // element type E2M1, code 1
+  const uint32_t afmt = fp4 ? 1u : (p.x2_format == GMMFR_E2M1 ? GMMFR_E4M3 : (uint32_t)p.x2_format);
+  const uint32_t bfmt = fp4 ? 1u : (p.x1_format == GMMFR_E2M1 ? GMMFR_E4M3 : (uint32_t)p.x1_format);
   gp.idesc = (1u << 23) | (afmt << 7) | (bfmt << 10) | ((128u >> 4) << 24);
   gp.timeout_ns = 4000000000ll;
   gp.test_stall = 0;

@@ -14,6 +14,10 @@ constexpr int kTileK = 128;                // K bytes per pipeline stage (4 MMAs
 constexpr int kWTileBytes = kTileN * kTileK;  // 16 KB of FP8 weights per tile
 constexpr int kSfChunk = 512;              // scale bytes of a 128-row x 4-block tile
 constexpr int kPrepTileBytes = kWTileBytes + kSfChunk;  // 16896: prepared tile = weights + scales
+// Packed E2M1 x E2M1 (kind::mxf4): the same 128-byte rows hold 256 K elements (two per
+// byte), so a stage carries 4 MMAs of K = 64 and 8 scales per row (two scale chunks).
+constexpr int kTileK4 = 256;                              // K elements per FP4 stage
+constexpr int kPrepTileBytes4 = kWTileBytes + 2 * kSfChunk;  // 17408
 constexpr int kTokBox = 16;                // token rows per TMA box
 constexpr int kGemmThreads = 224;          // warp 0 TMA, 1 MMA, 2..5 epilogue, 6 token-scale packer
 constexpr int kMaxExperts = 1024;
@@ -36,7 +40,8 @@ struct PrepParams {
   int32_t NT, KB, Ks;
   int32_t transpose_x2;
   int32_t scale_per_expert;
-  int32_t fp4;  // x2 holds packed E2M1 codes: expand to E4M3
+  int32_t fp4;         // x2 holds packed E2M1 codes
+  int32_t fp4_native;  // with fp4: keep them packed (256-K tiles for kind::mxf4), else expand to E4M3
 };
 cudaError_t launch_expand_fp4(const uint8_t* packed, uint8_t* fp8, int64_t n_bytes, cudaStream_t s);
 
@@ -74,6 +79,7 @@ struct GemmParams {
   int32_t deterministic;
   int32_t row_i32;
   int32_t tmax_fixed;      // 0: token group width chosen on the device from the largest expert
+  int32_t fp4;             // packed E2M1 tokens and weights: 256-K stages, kind::mxf4 MMAs
   uint32_t idesc;          // instruction descriptor without N and scale-factor ids
   int64_t timeout_ns;
   int32_t test_stall;      // testing aid: wait on a barrier nothing arrives on

@@ -143,6 +143,68 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepParams p) {
   }
 }
 
+// Packed E2M1 tile (e, j, kb) for kind::mxf4: 128 output columns n = j*128 + r by 256 K
+// elements k = kb*256 + 2c + h (byte c of row r, h = 0 low nibble, 1 high), swizzled as
+// above, then two 512-byte scale chunks: 32-block kb*8 + 4*h2 + q of row r at
+// 512*h2 + 16*(r%32) + 4*(r/32) + q.  Zero codes and 127 scales pad past N and K.
+__device__ void prep_tile_fp4(const PrepParams& p, int64_t e, int64_t j, int64_t kb, uint8_t* dst) {
+  const int64_t Ks = p.Ks;
+  const int64_t Kb = p.K / 2;  // packed bytes of one K row (K is even)
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int id = threadIdx.x + it * 256;
+    const int r = id & 127, c = id >> 7;
+    const int64_t n = j * kTileN + r;
+    const int64_t kk0 = kb * (kTileK4 / 2) + c * 16;  // first packed byte along K
+    uint8_t b[16];
+    if (p.transpose_x2) {  // x2 [E, N, K/2]: the bytes are already K pairs
+      const uint8_t* src = p.x2 + (e * p.N + n) * Kb + kk0;
+      if (n < p.N && kk0 + 16 <= Kb && ((reinterpret_cast<uintptr_t>(src) & 15) == 0)) {
+        *reinterpret_cast<uint4*>(b) = *reinterpret_cast<const uint4*>(src);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) b[i] = (n < p.N && kk0 + i < Kb) ? src[i] : 0;
+      }
+    } else {  // x2 [E, K, N/2]: nibble n&1 of rows k = 2kk and 2kk + 1
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uint32_t v = 0;
+        const int64_t kk = kk0 + i;
+        if (n < p.N && kk < Kb) {
+          const int sh = (int)(n & 1) * 4;
+          const uint32_t lo = (p.x2[(e * p.K + 2 * kk) * (p.N / 2) + n / 2] >> sh) & 15u;
+          const uint32_t hi = (p.x2[(e * p.K + 2 * kk + 1) * (p.N / 2) + n / 2] >> sh) & 15u;
+          v = lo | (hi << 4);
+        }
+        b[i] = (uint8_t)v;
+      }
+    }
+    *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = *reinterpret_cast<const uint4*>(b);
+  }
+  const int64_t sbase = p.scale_per_expert ? e * Ks * p.N * 2 : 0;
+  for (int id = threadIdx.x; id < 2 * kSfChunk; id += 256) {
+    const int r = id & 127, q = id >> 7;  // q = 0..7: 32-block within the 256-K block
+    const int64_t n = j * kTileN + r;
+    const int64_t g = kb * 8 + q;
+    uint8_t v = 127;
+    if (n < p.N && g * 32 < p.K) {
+      const int64_t kp = g >> 1, h = g & 1;
+      v = p.transpose_x2 ? p.scale[sbase + (n * Ks + kp) * 2 + h] : p.scale[sbase + (kp * p.N + n) * 2 + h];
+    }
+    dst[kWTileBytes + kSfChunk * (q >> 2) + 16 * (r & 31) + 4 * (r >> 5) + (q & 3)] = v;
+  }
+}
+
+__global__ void __launch_bounds__(256) prep_fp4_kernel(PrepParams p) {
+  const int64_t tiles = p.E * p.NT * p.KB;
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t kb = tile % p.KB;
+    const int64_t j = (tile / p.KB) % p.NT;
+    const int64_t e = tile / ((int64_t)p.KB * p.NT);
+    prep_tile_fp4(p, e, j, kb, p.prepared + tile * kPrepTileBytes4);
+  }
+}
+
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
   const int64_t tiles = p.E * p.NT * p.KB;
   if (tiles == 0) return cudaSuccess;
@@ -150,7 +212,10 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t grid = tiles < (int64_t)sms * 8 ? tiles : (int64_t)sms * 8;
-  prep_kernel<<<(unsigned)grid, 256, 0, s>>>(p);
+  if (p.fp4 && p.fp4_native)
+    prep_fp4_kernel<<<(unsigned)grid, 256, 0, s>>>(p);
+  else
+    prep_kernel<<<(unsigned)grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

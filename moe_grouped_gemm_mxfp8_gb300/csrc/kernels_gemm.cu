@@ -1,9 +1,11 @@
 // Persistent grouped GEMM of MXFP8 grouped-matmul-finalize-routing on sm_103a.
 //
 // Work: for every token group g (at most `tmax` routed tokens of one expert e),
-// every 128-column tile j of the output and every 128-element K block kb,
+// every 128-column tile j of the output and every K block kb of 128 bytes per row,
 //   D[n, t] += sum_{k in block} (x2[e,k,n] * s_w) * (x1[t,k] * s_x)
-// with tcgen05.mma kind::mxf8f6f4 block_scale (one E8M0 scale per 32 K).
+// with tcgen05.mma kind::mxf8f6f4 block_scale (FP8: 128 K elements per block), or
+// kind::mxf4 block_scale when tokens and weights are both packed E2M1 (256 K elements
+// per block, two per byte); one E8M0 scale per 32 K elements either way.
 // The weights are the 128-row A operand (rows = output columns), the tokens the
 // N-wide B operand (N = tokens rounded up to 16), so experts holding few tokens
 // still stream each weight byte exactly once.
@@ -43,23 +45,44 @@ namespace gmmfr {
 
 namespace cfg {
 // One ring of stages; a stage holds everything one K block of a segment needs:
-//   [0, 16384)        FP8 weight tile (1024-aligned, 128-byte swizzle)
-//   [16384, 16896)    its E8M0 scales (same bulk copy)
-//   [16896, 17408)    the token scales (packed by warp 6)
-//   [17408, ...)      tmax token rows of 128 bytes (1024-aligned, 128-byte swizzle)
+//   [0, 16384)        weight tile, 128 rows x 128 bytes (1024-aligned, 128-byte swizzle)
+//   [16384, +S)       its E8M0 scales (same bulk copy); S = 512 (FP8: 4 per row) or
+//                     1024 (packed E2M1: 8 per row, two 512-byte chunks)
+//   [16384 + S, +S)   the token scales (packed by warp 6), same layout
+//   [16384 + 2S, ...) tmax token rows of 128 bytes (1024-aligned, 128-byte swizzle)
 // Loaded L2 latency is about that of HBM here, so token rows need the same lead
 // time as weights and share the stage.
 constexpr int kMaxStages = 10;
 constexpr int kOffWSF = kWTileBytes;
-constexpr int kOffXSF = kWTileBytes + kSfChunk;
-constexpr int kOffX = kWTileBytes + 2 * kSfChunk;
-__host__ __device__ constexpr int stage_bytes(int tmax) { return kOffX + tmax * 128; }
-__host__ __device__ constexpr int n_stages(int tmax) { return tmax <= 32 ? 10 : (tmax <= 64 ? 8 : 6); }
-constexpr int kArena = 10 * 21504;  // 10 x 21504 (tmax 32), 8 x 25600 (64), 6 x 33792 (128)
-static_assert(n_stages(32) * stage_bytes(32) <= kArena && n_stages(64) * stage_bytes(64) <= kArena &&
-                  n_stages(128) * stage_bytes(128) <= kArena, "ring arena");
-constexpr int kTmemCols = 512;  // 2 x tmax accumulator columns + 8 scale columns per stage
-static_assert(2 * 128 + 8 * 6 <= kTmemCols && 2 * 64 + 8 * 8 <= kTmemCols && 2 * 32 + 8 * 10 <= kTmemCols, "TMEM");
+__host__ __device__ constexpr int sf_bytes(bool fp4) { return fp4 ? 2 * kSfChunk : kSfChunk; }
+__host__ __device__ constexpr int off_xsf(bool fp4) { return kWTileBytes + sf_bytes(fp4); }
+__host__ __device__ constexpr int off_x(bool fp4) { return kWTileBytes + 2 * sf_bytes(fp4); }
+__host__ __device__ constexpr int stage_bytes(int tmax, bool fp4) { return off_x(fp4) + tmax * 128; }
+__host__ __device__ constexpr int n_stages(int tmax, bool fp4) {
+  return tmax <= 32 ? (fp4 ? 9 : 10) : (tmax <= 64 ? 8 : 6);
+}
+// FP8: 10 x 21504 (tmax 32), 8 x 25600 (64), 6 x 33792 (128);
+// E2M1: 9 x 22528, 8 x 26624, 6 x 34816
+constexpr int kArena = 10 * 21504;
+static_assert(n_stages(32, false) * stage_bytes(32, false) <= kArena &&
+                  n_stages(64, false) * stage_bytes(64, false) <= kArena &&
+                  n_stages(128, false) * stage_bytes(128, false) <= kArena &&
+                  n_stages(32, true) * stage_bytes(32, true) <= kArena &&
+                  n_stages(64, true) * stage_bytes(64, true) <= kArena &&
+                  n_stages(128, true) * stage_bytes(128, true) <= kArena,
+              "ring arena");
+static_assert(off_x(true) % 1024 == 0 && stage_bytes(32, true) % 1024 == 0 && off_x(false) % 1024 == 0 &&
+                  stage_bytes(32, false) % 1024 == 0,
+              "swizzled operands need 1024-byte alignment");
+__host__ __device__ constexpr int sf_cols(bool fp4) { return fp4 ? 16 : 8; }  // TMEM scale columns per stage
+constexpr int kTmemCols = 512;  // 2 x tmax accumulator columns + the scale columns of every stage
+static_assert(2 * 128 + sf_cols(true) * n_stages(128, true) <= kTmemCols &&
+                  2 * 64 + sf_cols(true) * n_stages(64, true) <= kTmemCols &&
+                  2 * 32 + sf_cols(true) * n_stages(32, true) <= kTmemCols &&
+                  2 * 128 + sf_cols(false) * n_stages(128, false) <= kTmemCols &&
+                  2 * 64 + sf_cols(false) * n_stages(64, false) <= kTmemCols &&
+                  2 * 32 + sf_cols(false) * n_stages(32, false) <= kTmemCols,
+              "TMEM");
 constexpr int kNumBars = 2 * kMaxStages + 6;
 constexpr int kBarOff = kArena;
 constexpr int kEndOff = kBarOff + kNumBars * 8;              // int32 s_end[1024]
@@ -313,15 +336,18 @@ __device__ void shared_add_slice(const GemmParams& p, int ep_tid) {
   }
 }
 
-// The four E8M0 bytes of token t for the 32-element blocks 4*kb .. 4*kb+3
-// (blocks starting at or past K are padding: 127 = 1.0).
-__device__ __forceinline__ uint32_t token_scale_word(const GemmParams& p, int64_t t, int kb) {
-  const int64_t rowb = 2 * (int64_t)p.Ks;
-  const uint8_t* src = p.pertoken_scale + t * rowb + 4 * kb;
-  if ((rowb & 3) == 0 && (int64_t)(4 * kb + 3) * 32 < p.K) return *reinterpret_cast<const uint32_t*>(src);
+// The four E8M0 bytes of token t for the 32-element blocks 4*c .. 4*c+3 (c = kb for FP8
+// blocks, 2*kb and 2*kb + 1 for the two halves of a packed E2M1 block); blocks starting at
+// or past K are padding: 127 = 1.0.
+__device__ __forceinline__ bool scale_words_aligned(const GemmParams& p) {
+  return ((reinterpret_cast<uintptr_t>(p.pertoken_scale) | (uintptr_t)(2 * p.Ks)) & 3) == 0;
+}
+__device__ __forceinline__ uint32_t token_scale_word(const GemmParams& p, int64_t t, int c) {
+  const uint8_t* src = p.pertoken_scale + t * 2 * (int64_t)p.Ks + 4 * c;
+  if (scale_words_aligned(p) && (int64_t)(4 * c + 3) * 32 < p.K) return *reinterpret_cast<const uint32_t*>(src);
   uint32_t w = 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) w |= ((int64_t)(4 * kb + q) * 32 < p.K ? (uint32_t)src[q] : 127u) << (8 * q);
+  for (int q = 0; q < 4; ++q) w |= ((int64_t)(4 * c + q) * 32 < p.K ? (uint32_t)src[q] : 127u) << (8 * q);
   return w;
 }
 
@@ -348,16 +374,24 @@ __device__ __forceinline__ bool pack_next(PackIter& it, Sched& sched, const Grou
   return false;
 }
 
-// Scale words of tokens lane, lane+32, lane+64, lane+96 of the item (127 = 1.0 past the group).
-__device__ __forceinline__ void pack_load(const GemmParams& p, const PackIter& it, uint32_t (&w)[4]) {
+// Scale words of tokens lane, lane+32, lane+64, lane+96 of the item (127 = 1.0 past the
+// group): w[r] for the item's 32-blocks 0..3, and with packed E2M1 w[4 + r] for 4..7.
+template <bool fp4>
+__device__ __forceinline__ void pack_load(const GemmParams& p, const PackIter& it, uint32_t (&w)[8]) {
   const int lane = threadIdx.x & 31;
+  const int c = fp4 ? 2 * it.kb : it.kb;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int i = lane + 32 * r;
-    w[r] = (it.valid && i < it.T) ? token_scale_word(p, (int64_t)it.t0 + i, it.kb) : 0x7F7F7F7Fu;
+    const bool in = it.valid && i < it.T;
+    w[r] = in ? token_scale_word(p, (int64_t)it.t0 + i, c) : 0x7F7F7F7Fu;
+    w[4 + r] = (fp4 && in) ? token_scale_word(p, (int64_t)it.t0 + i, c + 1) : 0x7F7F7F7Fu;
   }
 }
 
+// fp4: packed E2M1 operands (kind::mxf4); a separate instantiation keeps each format's
+// loops free of the other's code.
+template <bool fp4>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ TokenMaps tmaps, const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -413,8 +447,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const Groups groups{s_end, s_gbase, s_wbase, p.E, tmax};
-  const int stage_bytes = cfg::stage_bytes(tmax);
-  const int n_stages = cfg::n_stages(tmax);
+  const int stage_bytes = cfg::stage_bytes(tmax, fp4);
+  const int n_stages = cfg::n_stages(tmax, fp4);
+  const int off_xsf = cfg::off_xsf(fp4), off_x = cfg::off_x(fp4);
   const Ctl ctl{abort_flag, s_err, p.timeout_ns};
   Sched sched;
   sched.init(n_groups, p.NT, p.KB, p.deterministic != 0, p.split, groups);
@@ -439,8 +474,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int t0, T;
         groups.info(sg.g, e, t0, T);
         const int m = (T + 15) / 16;  // token rows in 16-row units: boxes of 128/64/32/16 rows
-        const uint32_t tx = kPrepTileBytes + m * 16 * 128;
-        const uint8_t* wsrc = p.prepared + ((int64_t)e * p.NT + sg.j) * p.KB * (int64_t)kPrepTileBytes;
+        const int ptile = fp4 ? kPrepTileBytes4 : kPrepTileBytes;
+        const uint32_t tx = ptile + m * 16 * 128;
+        const uint8_t* wsrc = p.prepared + ((int64_t)e * p.NT + sg.j) * p.KB * (int64_t)ptile;
         // sibling groups of the same expert read the same weight tiles shortly after
         const uint64_t pol_w = (s_gbase[e + 1] - s_gbase[e]) > 1 ? pol_keep : pol_stream;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
@@ -451,20 +487,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fb = ptx::smem_u32(&full[stage]);
           const uint32_t sb = smem_base + stage * stage_bytes;
           ptx::mbar_arrive_expect_tx(fb, tx);
-          ptx::bulk_g2s(sb, wsrc + (int64_t)kb * kPrepTileBytes, kPrepTileBytes, fb, pol_w);
+          ptx::bulk_g2s(sb, wsrc + (int64_t)kb * ptile, ptile, fb, pol_w);
           // token rows: one 128-row box, or a 64-row box, then 32-row boxes and a
           // last 16-row box for an odd count (measured fastest on this part)
           int row = 0;
           if (m == 8) {
-            ptx::tma_load_2d(sb + cfg::kOffX, &tmaps.m[3], kb * kTileK, t0, fb, pol_keep);
+            ptx::tma_load_2d(sb + off_x, &tmaps.m[3], kb * kTileK, t0, fb, pol_keep);
             row = 128;
           } else if (m > 4) {
-            ptx::tma_load_2d(sb + cfg::kOffX, &tmaps.m[2], kb * kTileK, t0, fb, pol_keep);
+            ptx::tma_load_2d(sb + off_x, &tmaps.m[2], kb * kTileK, t0, fb, pol_keep);
             row = 64;
           }
           for (; row < m * 16; row += 32) {
             const int last16 = row + 16 == m * 16;
-            ptx::tma_load_2d(sb + cfg::kOffX + row * 128, &tmaps.m[last16 ? 0 : 1], kb * kTileK, t0 + row, fb,
+            ptx::tma_load_2d(sb + off_x + row * 128, &tmaps.m[last16 ? 0 : 1], kb * kTileK, t0 + row, fb,
                              pol_keep);
           }
           ++fills[stage];
@@ -510,16 +546,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t sb = smem_base + stage * stage_bytes;
-          const uint32_t sfa = tmem_base + 2 * tmax + stage * 8;  // per-stage scale columns
-          const uint32_t sfb = sfa + 4;
-          ptx::tc_cp_sf(sfa, ptx::smem_desc(sb + cfg::kOffWSF, 0, 128, ptx::kSwizzleNone));
-          ptx::tc_cp_sf(sfb, ptx::smem_desc(sb + cfg::kOffXSF, 0, 128, ptx::kSwizzleNone));
+          const uint32_t sfa = tmem_base + 2 * tmax + stage * cfg::sf_cols(fp4);  // per-stage scale columns
+          if constexpr (fp4) {
+            // two scale chunks per operand (32-blocks 0..3 and 4..7 of the 256-K block); MMA q
+            // covers 32-blocks 2q, 2q + 1: chunk q / 2, bytes 2 (q % 2) and 2 (q % 2) + 1
+            const uint32_t sfb = sfa + 8;
+            ptx::tc_cp_sf(sfa, ptx::smem_desc(sb + cfg::kOffWSF, 0, 128, ptx::kSwizzleNone));
+            ptx::tc_cp_sf(sfa + 4, ptx::smem_desc(sb + cfg::kOffWSF + kSfChunk, 0, 128, ptx::kSwizzleNone));
+            ptx::tc_cp_sf(sfb, ptx::smem_desc(sb + off_xsf, 0, 128, ptx::kSwizzleNone));
+            ptx::tc_cp_sf(sfb + 4, ptx::smem_desc(sb + off_xsf + kSfChunk, 0, 128, ptx::kSwizzleNone));
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint64_t adesc = ptx::smem_desc(sb + 32 * q, 16, 1024, ptx::kSwizzle128B);
-            const uint64_t bdesc = ptx::smem_desc(sb + cfg::kOffX + 32 * q, 16, 1024, ptx::kSwizzle128B);
-            const uint32_t id = idesc | ((uint32_t)q << 4) | ((uint32_t)q << 29);
-            ptx::tc_mma_mxf8(d_tmem, adesc, bdesc, id, sfa, sfb, (kb > sg.kb0 || q > 0) ? 1u : 0u);
+            for (int q = 0; q < 4; ++q) {
+              const uint64_t adesc = ptx::smem_desc(sb + 32 * q, 16, 1024, ptx::kSwizzle128B);
+              const uint64_t bdesc = ptx::smem_desc(sb + off_x + 32 * q, 16, 1024, ptx::kSwizzle128B);
+              const uint32_t sid = 2u * (uint32_t)(q & 1);
+              const uint32_t id = idesc | (sid << 4) | (sid << 29);
+              const uint32_t col = 4u * (uint32_t)(q >> 1);
+              ptx::tc_mma_mxf4(d_tmem, adesc, bdesc, id, sfa + col, sfb + col, (kb > sg.kb0 || q > 0) ? 1u : 0u);
+            }
+          } else {
+            const uint32_t sfb = sfa + 4;
+            ptx::tc_cp_sf(sfa, ptx::smem_desc(sb + cfg::kOffWSF, 0, 128, ptx::kSwizzleNone));
+            ptx::tc_cp_sf(sfb, ptx::smem_desc(sb + off_xsf, 0, 128, ptx::kSwizzleNone));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint64_t adesc = ptx::smem_desc(sb + 32 * q, 16, 1024, ptx::kSwizzle128B);
+              const uint64_t bdesc = ptx::smem_desc(sb + off_x + 32 * q, 16, 1024, ptx::kSwizzle128B);
+              const uint32_t id = idesc | ((uint32_t)q << 4) | ((uint32_t)q << 29);
+              ptx::tc_mma_mxf8(d_tmem, adesc, bdesc, id, sfa, sfb, (kb > sg.kb0 || q > 0) ? 1u : 0u);
+            }
           }
           ptx::tc_commit(ptx::smem_u32(&empty[stage]));
           if (++stage == n_stages) {
@@ -544,20 +599,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     PackIter it;
     it.valid = false;
     it.e = -1;
-    uint32_t w0[4], w1[4], w2[4];
+    uint32_t w0[8], w1[8], w2[8];
     bool v0 = pack_next(it, sched, groups);
-    pack_load(p, it, w0);
+    pack_load<fp4>(p, it, w0);
     bool v1 = v0 && pack_next(it, sched, groups);
-    pack_load(p, it, w1);
+    pack_load<fp4>(p, it, w1);
     bool v2 = v1 && pack_next(it, sched, groups);
-    pack_load(p, it, w2);
+    pack_load<fp4>(p, it, w2);
     int stage = 0;
     uint32_t phase = 0;
     while (v0) {
       if (!warp_wait_bar(ptx::smem_u32(&empty[stage]), phase ^ 1, ctl)) break;
-      uint8_t* xsf = smem + stage * stage_bytes + cfg::kOffXSF;
+      uint8_t* xsf = smem + stage * stage_bytes + off_xsf;
 #pragma unroll
       for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t*>(xsf + 16 * lane + 4 * r) = w0[r];
+      if constexpr (fp4) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t*>(xsf + kSfChunk + 16 * lane + 4 * r) = w0[4 + r];
+      }
       ptx::fence_proxy_async_smem();  // make the generic-proxy stores visible to tcgen05.cp
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&full[stage]));
@@ -566,14 +625,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         phase ^= 1;
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < 8; ++r) {
         w0[r] = w1[r];
         w1[r] = w2[r];
       }
       v0 = v1;
       v1 = v2;
       v2 = v2 && pack_next(it, sched, groups);
-      pack_load(p, it, w2);
+      pack_load<fp4>(p, it, w2);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -616,18 +675,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acce[buf]));
         }
         const int cnt = T - c0 < 32 ? T - c0 : 32;
+        // one unrolled loop per mode, so the atomic mode's hot code holds no store path of
+        // the deterministic one (the instruction cache is the scarce resource here)
+        if (p.deterministic) {
+          float* y = p.ybuf + ((int64_t)sg.slot * p.M + t0 + c0) * p.N + n;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          if (jj < cnt) {
-            const int row = __shfl_sync(0xffffffffu, my_row, jj);
-            const float lg = __shfl_sync(0xffffffffu, my_lg, jj);
-            const float val = (__uint_as_float(v[jj]) + bias_n) * lg;
-            if (n_ok) {
-              if (p.deterministic) {
-                p.ybuf[((int64_t)sg.slot * p.M + t0 + c0 + jj) * p.N + n] = val;
-              } else if (row >= 0) {
-                ptx::red_add_f32(p.out + (int64_t)row * p.N + n, val);
-              }
+          for (int jj = 0; jj < 32; ++jj) {
+            if (jj < cnt) {
+              const float lg = __shfl_sync(0xffffffffu, my_lg, jj);
+              if (n_ok) y[(int64_t)jj * p.N] = (__uint_as_float(v[jj]) + bias_n) * lg;
+            }
+          }
+        } else {
+          float* o = p.out + n;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            if (jj < cnt) {
+              const int row = __shfl_sync(0xffffffffu, my_row, jj);
+              const float lg = __shfl_sync(0xffffffffu, my_lg, jj);
+              if (n_ok && row >= 0) ptx::red_add_f32(o + (int64_t)row * p.N, (__uint_as_float(v[jj]) + bias_n) * lg);
             }
           }
         }
@@ -661,7 +727,9 @@ cudaError_t launch_gemm(const TokenMaps& tmaps, const GemmParams& p, int grid, c
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
@@ -678,7 +746,7 @@ cudaError_t launch_gemm(const TokenMaps& tmaps, const GemmParams& p, int grid, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, gemm_kernel, tmaps, p);
+  return p.fp4 ? cudaLaunchKernelEx(&lc, gemm_kernel<true>, tmaps, p) : cudaLaunchKernelEx(&lc, gemm_kernel<false>, tmaps, p);
 }
 
 }  // namespace gmmfr

@@ -138,14 +138,24 @@ def test_sizes_follow_the_tiling(lib):
 
 
 def test_e2m1_sizes_and_parity_rules(lib):
-    """MXFP4: an odd N is allowed when x2 is transposed (packed along K); E2M1
-    tokens add M*K bytes of workspace for their E4M3 expansion; the prepared
-    weights are the FP8 tiles whatever the input format."""
+    """MXFP4: an odd N is allowed when x2 is transposed (packed along K).  E2M1 tokens
+    and weights with K % 32 == 0 stay packed: tiles of 256 K elements (17408 bytes with
+    their eight scales per row) and no token expansion.  Otherwise E2M1 tokens add M*K
+    bytes of workspace for their E4M3 expansion and the weights become the FP8 tiles."""
     base = _ok_problem()
     n8 = B.gmmfr_workspace_size(base, True)
     p4 = _ok_problem(x1_format=2, x2_format=2)
-    assert B.gmmfr_workspace_size(p4, True) >= n8 + p4.M * p4.K
-    assert B.gmmfr_prepared_weights_size(p4) == B.gmmfr_prepared_weights_size(base)
+    assert B.gmmfr_workspace_size(p4, True) == n8
+    assert B.gmmfr_prepared_weights_size(p4) == p4.E * (-(-p4.N // 128)) * (-(-p4.K // 256)) * 17408
+    assert B.gmmfr_workspace_size(p4, False) == n8 + B.gmmfr_prepared_weights_size(p4)
+    for kw in (dict(x1_format=2, x2_format=0), dict(x1_format=2, x2_format=2, K=5120 + 16)):
+        pm = _ok_problem(**kw)
+        p8 = _ok_problem(K=pm.K)
+        assert B.gmmfr_workspace_size(pm, True) >= B.gmmfr_workspace_size(p8, True) + pm.M * pm.K
+        assert B.gmmfr_prepared_weights_size(pm) == B.gmmfr_prepared_weights_size(p8)
+    p_w = _ok_problem(x2_format=2)  # FP8 tokens, E2M1 weights: FP8 tiles, no token workspace
+    assert B.gmmfr_workspace_size(p_w, True) == n8
+    assert B.gmmfr_prepared_weights_size(p_w) == B.gmmfr_prepared_weights_size(base)
     B.gmmfr_workspace_size(_ok_problem(x2_format=2, N=63, transpose_x2=1), True)
     B.gmmfr_workspace_size(_ok_problem(x1_format=2, N=63), True)
 

@@ -156,9 +156,17 @@ SMALL = {
     "bias_split_k": dict(E=4, M=60, N=320, K=1024, bias=True, rows="random", out_init="randn"),
     "bias_wide": dict(E=3, M=300, batch=64, N=256, K=256, bias=True, counts="explicit",
                       explicit_counts=(150, 0, 150), rows="random", transpose_x2=True),
-    # MXFP4 (E2M1 codes two per byte, expanded exactly to E4M3 before the MMA)
+    # MXFP4 (E2M1 codes two per byte): tokens and weights both E2M1 with K % 32 == 0 stay packed
+    # (kind::mxf4, 256 K per tile); other E2M1 operands are expanded exactly to E4M3
     "mxfp4": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1),
     "mxfp4_t": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, transpose_x2=True, rows="random"),
+    "mxfp4_k352_bias": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, K=352, N=200, bias=True, rows="random",
+                            out_init="randn"),                 # two K tiles, the second 96 of 256 long
+    "mxfp4_k96": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, K=96, N=130, transpose_x2=True,
+                      scale_per_expert=True),                  # one partial tile, padding scale block
+    "mxfp4_k1024_split": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, E=4, M=60, N=320, K=1024, bias=True,
+                              rows="random", out_init="randn"),  # K tiles of one column tile split over CTAs
+    "mxfp4_k48_expanded": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, K=48, N=64),  # K % 32 != 0: expanded
     "mxfp4_tokens_e5m2_weights": dict(x1_dtype=W.E2M1, x2_dtype=W.E5M2, K=96),
     "e4m3_tokens_mxfp4_weights": dict(x2_dtype=W.E2M1, transpose_x2=True, scale_per_expert=True, bias=True,
                                       N=255),
@@ -175,7 +183,7 @@ def test_small_atomic(name):
 
 
 @pytest.mark.parametrize("name", ["basic", "transposed", "ragged_counts", "random_rows_shared", "straddle", "k96",
-                                  "bias_split_k", "mxfp4_t"])
+                                  "bias_split_k", "mxfp4_t", "mxfp4_k352_bias"])
 def test_small_deterministic(name):
     spec = _spec(**SMALL[name])
     inp = W.make_inputs(spec)
@@ -286,12 +294,12 @@ def test_prepared_layout_round_trip():
 
 
 def test_prepared_e2m1_equals_prepared_e4m3_widening():
-    """E2M1 weights are prepared as the E4M3 tiles of the same values: the prepared
-    buffer of packed FP4 x2 is byte-identical to that of x2 widened to one E4M3
-    byte per element (the widening done here with torch's float8 cast)."""
+    """E2M1 weights paired with FP8 tokens are prepared as the E4M3 tiles of the same
+    values: the prepared buffer of packed FP4 x2 is byte-identical to that of x2 widened
+    to one E4M3 byte per element (the widening done here with torch's float8 cast)."""
     table = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
     for transpose in (False, True):
-        spec = _spec(K=208, N=200, E=2, transpose_x2=transpose, x1_dtype=W.E2M1, x2_dtype=W.E2M1)
+        spec = _spec(K=208, N=200, E=2, transpose_x2=transpose, x1_dtype=W.E4M3, x2_dtype=W.E2M1)
         inp = W.make_inputs(spec)
         x2 = inp["x2"]
         codes = torch.stack([x2 & 15, x2 >> 4], dim=-1).reshape(*x2.shape[:-1], -1).long()
@@ -302,6 +310,47 @@ def test_prepared_e2m1_equals_prepared_e4m3_widening():
         p4 = B.prepare_weights(prob4, x2.cuda(), sc).cpu()
         p8 = B.prepare_weights(prob8, wide.cuda(), sc).cpu()
         assert p4.numel() == p8.numel() and torch.equal(p4, p8)
+
+
+def test_prepared_packed_e2m1_layout_round_trip():
+    """E2M1 tokens and weights: the prepared tiles keep the codes packed, K pairs per byte
+    (element k = 256 kb + 2c in the low nibble of byte c, k + 1 in the high nibble),
+    swizzled as the FP8 tiles, then eight scales per row in two 512-byte chunks
+    (bit-exact byte work), for both x2 layouts."""
+    for transpose in (False, True):
+        spec = _spec(K=352, N=200, E=2, transpose_x2=transpose, x1_dtype=W.E2M1, x2_dtype=W.E2M1)
+        inp = W.make_inputs(spec)
+        prob = B.problem_from_spec(spec)
+        buf = B.prepare_weights(prob, inp["x2"].cuda(), inp["scale"].cuda()).cpu().numpy()
+        E, K, N = spec.E, spec.K, spec.N
+        NT, KB, Ks = -(-N // 128), -(-K // 256), spec.Ks
+        assert buf.size >= E * NT * KB * 17408
+        tiles = buf[:E * NT * KB * 17408].reshape(E, NT, KB, 17408)
+        x2 = inp["x2"].numpy().astype(np.int64)
+        # codes as [E, K, N]
+        if transpose:  # [E, N, K/2], packed along K
+            codes = np.stack([x2 & 15, x2 >> 4], axis=-1).reshape(E, N, K).transpose(0, 2, 1)
+        else:          # [E, K, N/2], packed along N
+            codes = np.stack([x2 & 15, x2 >> 4], axis=-1).reshape(E, K, N)
+        sc = inp["scale"].numpy()
+        r = np.arange(128)[:, None]
+        c = np.arange(128)[None, :]
+        for e in range(E):
+            for j in range(NT):
+                for kb in range(KB):
+                    t = tiles[e, j, kb]
+                    byte = t[(r * 128 + (((c // 16) ^ (r % 8)) * 16) + c % 16)].astype(np.int64)
+                    n, k = j * 128 + r, kb * 256 + 2 * c
+                    ok = (n < N) & (k < K)
+                    nn, kk = np.minimum(n, N - 1), np.minimum(k, K - 2)
+                    assert np.array_equal(byte & 15, np.where(ok, codes[e, kk, nn], 0))
+                    assert np.array_equal(byte >> 4, np.where(ok, codes[e, kk + 1, nn], 0))
+                    q = np.arange(8)[None, :]
+                    s = t[16384 + 512 * (q // 4) + 16 * (r % 32) + 4 * (r // 32) + q % 4]
+                    g = kb * 8 + q
+                    kp, h = np.minimum(g // 2, Ks - 1), g % 2
+                    sv = sc[kp, nn, h] if not transpose else sc[nn, kp, h]
+                    assert np.array_equal(s, np.where((n < N) & (g * 32 < K), sv, 127))
 
 
 def test_timeout_path_reports_and_recovers(monkeypatch):
