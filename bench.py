@@ -144,13 +144,14 @@ class ClockSampler:
 
 def _oracle_problem(spec, inp, ncols):
     import oracle
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
     x2 = inp["x2"].cpu()
     sc = inp["scale"].cpu()
     if spec.transpose_x2:
         x2s = x2[:, :ncols, :].contiguous()
         scs = sc[..., :ncols, :, :].contiguous()
-    else:
-        x2s = x2[:, :, :ncols].contiguous()
+    else:  # [E, K, N]; E2M1 holds two columns per byte along N (ncols is even)
+        x2s = x2[:, :, :(ncols // 2 if spec.x2_dtype == W.E2M1 else ncols)].contiguous()
         scs = sc[..., :ncols, :].contiguous()
     shared = inp["shared_input"][:, :ncols].contiguous() if inp["shared_input"] is not None else None
     return oracle.Problem(M=spec.M, K=spec.K, N=ncols, E=spec.E, batch=spec.batch, x1=inp["x1"].cpu(), x2=x2s,
@@ -394,7 +395,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    spec = W.config(args.config)
+    spec = _main_spec(args)
     inp = W.make_inputs(spec)
     counts = W.expert_counts(spec)
     vals = []
@@ -415,6 +416,18 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _main_spec(args):
+    """The workload of the timed call: --config N, or with --fp4 the MXFP4 operator at the
+    large shape (c5) or its reduced copy (e32)."""
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+    if args.fp4 == "c5":
+        return W.mxfp4_config()
+    if args.fp4 == "e32":
+        return W.mxfp4_small_config()
+    return W.config(args.config)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -432,7 +445,7 @@ def run_ours(args):
     build_mod.build()
     B.load()
 
-    spec = W.config(args.config)
+    spec = _main_spec(args)
     counts = W.expert_counts(spec)
     alg_bytes = W.algorithmic_bytes(spec, counts)
     flops = W.flops(spec, counts)
@@ -546,7 +559,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "mxfp8 (fp8 x fp8, e8m0 per 32) -> f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": ("mxfp4 (e2m1 x e2m1, e8m0 per 32) -> f32" if spec.x1_dtype == W.E2M1 and spec.x2_dtype == W.E2M1
+                  else "mxfp8 (fp8 x fp8, e8m0 per 32) -> f32"), "data": "synthetic",
         "config": _config_dict(spec, counts, args.deterministic),
         "us_per_call": ms * 1e3, "us_per_call_min": min(call_ms) * 1e3,
         "us_per_call_p10_p50_p90": [round(float(x) * 1e3, 2) for x in _quantiles(call_ms, (0.1, 0.5, 0.9))],
@@ -587,6 +601,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--fp4", default="off", choices=["off", "c5", "e32"],
+                    help="time the MXFP4 (E2M1) operator instead: the large shape, or its 32-expert copy")
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

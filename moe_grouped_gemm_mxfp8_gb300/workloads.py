@@ -239,6 +239,13 @@ def mxfp4_config() -> Spec:
                                seed=1105)
 
 
+def mxfp4_small_config() -> Spec:
+    """A reduced copy of the MXFP4 large workload (same K, N, tokens per expert and routing
+    recipe, 32 experts: 0.5 GB of prepared FP4 weights), sized for full profiler captures."""
+    return Spec("MXFP4-E32 M512 K7168 N4096 E32", batch=64, M=512, K=7168, N=4096, E=32, counts="multinomial",
+                rows="topk", topk=8, logit="softmax", x1_dtype=E2M1, x2_dtype=E2M1, seed=1106)
+
+
 def algorithmic_bytes(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:
     """Bytes a single call must move at minimum: x2 (and its scales) of every
     expert that holds a token, x1, pertoken_scale, logit, row_index,

@@ -353,6 +353,25 @@ def test_prepared_packed_e2m1_layout_round_trip():
                     assert np.array_equal(s, np.where((n < N) & (g * 32 < K), sv, 127))
 
 
+@pytest.mark.parametrize("offset", [1, 4])
+def test_unaligned_pertoken_scale(offset):
+    """pertoken_scale at a base that is not 4-byte aligned (offset 1: the packer assembles each
+    scale word from bytes) or only 4-byte aligned (offset 4: whole-word loads)."""
+    spec = _spec(K=1024, N=256, M=40, E=4, rows="random")
+    inp = W.make_inputs(spec)
+    d = _dev(inp)
+    ps = d["pertoken_scale"]
+    buf = torch.zeros(ps.numel() + 32, dtype=torch.uint8, device="cuda")
+    view = buf[offset:offset + ps.numel()].view(ps.shape)
+    view.copy_(ps)
+    d["pertoken_scale"] = view
+    got, bits = gpu_run(spec, inp, d=d)
+    ref, absb, flags = oracle.run(oracle.problem_from_spec(spec, inp))
+    init, sh = _extra_terms(spec, inp)
+    assert_close(got, ref, oracle.tolerance(ref, absb, init, sh))
+    assert bits == flags
+
+
 def test_timeout_path_reports_and_recovers(monkeypatch):
     """A wait that nothing completes gives up after its limit, reports
     GMMFR_DEV_TIMEOUT, and leaves the context usable."""
