@@ -19,7 +19,9 @@ constexpr int kPrepTileBytes = kWTileBytes + kSfChunk;  // 16896: prepared tile 
 constexpr int kTileK4 = 256;                              // K elements per FP4 stage
 constexpr int kPrepTileBytes4 = kWTileBytes + 2 * kSfChunk;  // 17408
 constexpr int kTokBox = 16;                // token rows per TMA box
-constexpr int kGemmThreads = 224;          // warp 0 TMA, 1 MMA, 2..5 epilogue, 6 token-scale packer
+// warp 0 TMA, 1 MMA, 2..5 epilogue, then the token-scale packers: one for FP8 operands, two
+// for packed E2M1 (eight scale words per lane per stage)
+__host__ __device__ constexpr int gemm_threads(bool fp4) { return fp4 ? 256 : 224; }
 constexpr int kMaxExperts = 1024;
 
 // Workspace header: word 0 = number of error slots written by the last GEMM

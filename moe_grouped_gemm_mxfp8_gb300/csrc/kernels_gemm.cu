@@ -16,7 +16,7 @@
 // few weight tiles as possible), and the first group of every expert.  The
 // shared-memory ring is then cut into as many stages as fit for that width.
 //
-// Roles (224 threads, one CTA per SM):
+// Roles (224 threads for FP8 operands, 256 for packed E2M1; one CTA per SM):
 //   warp 0     TMA producer: prepared weight tile + its scales (one bulk copy) and
 //              the token rows (boxes of 128, 64, 32 or 16 rows)
 //   warp 1     TMEM owner and MMA issuer (scale copies to TMEM, 4 MMAs per stage)
@@ -24,8 +24,9 @@
 //              out[row_index[t], n] (or a plain store into the per-token buffer in
 //              deterministic mode); before the first tile they add the shared
 //              input for their slice of rows.
-//   warp 6     token-scale packer: pertoken_scale bytes of the stage's tokens into
-//              the 32-row x 16-byte layout tcgen05.cp spreads over TMEM lanes.
+//   warp 6     token-scale packer: pertoken_scale bytes of the stage's tokens into the
+//              32-row x 16-byte layout tcgen05.cp spreads over TMEM lanes; with packed
+//              E2M1 warps 6 and 7 take the even and odd stages.
 //
 // Scheduling: atomic mode splits the total (group, tile, K-block) iteration space
 // over the CTAs in contiguous ranges (stream-K) of equal item count, or, when token
@@ -89,6 +90,7 @@ constexpr int kEndOff = kBarOff + kNumBars * 8;              // int32 s_end[1024
 constexpr int kGbaseOff = kEndOff + 4 * kMaxExperts;         // int32 s_gbase[1025]
 constexpr int kWbaseOff = kGbaseOff + 4 * (kMaxExperts + 4); // int32 s_wbase[1025]
 constexpr int kScanOff = kWbaseOff + 4 * (kMaxExperts + 4);  // int64 scan scratch[8]
+static_assert(gemm_threads(true) <= 8 * 32 && gemm_threads(false) <= 8 * 32, "scan scratch: one word per warp");
 constexpr int kMiscOff = kScanOff + 8 * 8;                   // int32 misc[8]
 constexpr int kSmemBytes = kMiscOff + 32 + 1024;             // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -244,26 +246,27 @@ __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uin
 // needed.  Fills s_end, chooses tmax, fills s_gbase.  Returns the group count.
 // g0 = group_list[threadIdx.x] (0 past E), loaded by the caller at kernel entry so that
 // its latency overlaps the barrier and TMEM set-up.
+template <int kThreads>
 __device__ int decode_groups(const GemmParams& p, int64_t g0, int32_t* s_end, int32_t* s_gbase, int32_t* s_wbase,
                              int64_t* scratch, uint32_t* s_err, int& tmax_out) {
   const int E = p.E;
   const int64_t M = p.M;
   const int tid = threadIdx.x;
   int64_t carry = 0;
-  for (int base = 0; base < E; base += kGemmThreads) {  // uniform trip count
+  for (int base = 0; base < E; base += kThreads) {  // uniform trip count
     const int e = base + tid;
     const int64_t g = base == 0 ? g0 : (e < E ? p.group_list[e] : 0);
     int64_t v, tot;
     if (p.group_list_type == 1) {
       if (e < E && g < 0) atomicOr(s_err, kErrBadGroupList);
       const int64_t c = e < E ? (g < 0 ? 0 : (g > M ? M + 1 : g)) : 0;
-      v = cta_scan<false, kGemmThreads>(c, scratch, tot) + carry;
+      v = cta_scan<false, kThreads>(c, scratch, tot) + carry;
       carry += tot;
     } else {
       const int64_t prev = (e > 0 && e < E) ? p.group_list[e - 1] : 0;
       if (e < E && (g < prev || g > M)) atomicOr(s_err, kErrBadGroupList);
       const int64_t c = e < E ? (g < 0 ? 0 : (g > M ? M : g)) : 0;
-      v = cta_scan<true, kGemmThreads>(c, scratch, tot);
+      v = cta_scan<true, kThreads>(c, scratch, tot);
       v = v > carry ? v : carry;
       carry = tot > carry ? tot : carry;
     }
@@ -273,28 +276,28 @@ __device__ int decode_groups(const GemmParams& p, int64_t g0, int32_t* s_end, in
   __syncthreads();
   // largest expert -> token group width
   int64_t mx = 0;
-  for (int e = tid; e < E; e += kGemmThreads) {
+  for (int e = tid; e < E; e += kThreads) {
     const int64_t c = s_end[e] - (e ? s_end[e - 1] : 0);
     mx = c > mx ? c : mx;
   }
   int64_t mx_all;
-  cta_scan<true, kGemmThreads>(mx, scratch, mx_all);
+  cta_scan<true, kThreads>(mx, scratch, mx_all);
   int tmax = mx_all <= 32 ? 32 : (mx_all <= 64 ? 64 : 128);
   if (p.tmax_fixed) tmax = p.tmax_fixed;
   // first group of every expert, and (when groups can differ much in size) the cost prefix
   // of the experts' items
   const bool weigh = tmax >= 64;
   int64_t gcarry = 0, wcarry = 0;
-  for (int base = 0; base < E; base += kGemmThreads) {
+  for (int base = 0; base < E; base += kThreads) {
     const int e = base + tid;
     const int64_t c = e < E ? s_end[e] - (e ? s_end[e - 1] : 0) : 0;
     const int64_t ng = (c + tmax - 1) / tmax;
     const int64_t w = ng > 0 ? (ng - 1) * item_cost(tmax) + item_cost((int)(c - (ng - 1) * tmax)) : 0;
     int64_t tot, wtot;
-    const int64_t incl = cta_scan<false, kGemmThreads>(ng, scratch, tot) + gcarry;
+    const int64_t incl = cta_scan<false, kThreads>(ng, scratch, tot) + gcarry;
     int64_t wincl = 0;
     wtot = 0;
-    if (weigh) wincl = cta_scan<false, kGemmThreads>(w, scratch, wtot) + wcarry;  // uniform branch
+    if (weigh) wincl = cta_scan<false, kThreads>(w, scratch, wtot) + wcarry;  // uniform branch
     if (e < E) {
       s_gbase[e] = (int32_t)(incl - ng);
       s_wbase[e] = (int32_t)((wincl - w) < INT32_MAX ? wincl - w : INT32_MAX);
@@ -392,7 +395,7 @@ __device__ __forceinline__ void pack_load(const GemmParams& p, const PackIter& i
 // fp4: packed E2M1 operands (kind::mxf4); a separate instantiation keeps each format's
 // loops free of the other's code.
 template <bool fp4>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(fp4), 1)
     gemm_kernel(const __grid_constant__ TokenMaps tmaps, const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   __syncthreads();
   int tmax;
-  const int n_groups = decode_groups(p, g0, s_end, s_gbase, s_wbase, s_scan, s_err, tmax);
+  const int n_groups = decode_groups<gemm_threads(fp4)>(p, g0, s_end, s_gbase, s_wbase, s_scan, s_err, tmax);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -591,48 +594,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       wait_bar_drain(ptx::smem_u32(drain), 0);
     }
     __syncwarp();
-  } else if (warp == 6) {
-    // ------------------------------------------------------------ token-scale packer
-    // Walks the (segment, K block) items in stage order; an item's scale words
-    // are loaded three items before its stage is filled, so L2 latency overlaps
-    // the ring.
-    PackIter it;
-    it.valid = false;
-    it.e = -1;
-    uint32_t w0[8], w1[8], w2[8];
-    bool v0 = pack_next(it, sched, groups);
-    pack_load<fp4>(p, it, w0);
-    bool v1 = v0 && pack_next(it, sched, groups);
-    pack_load<fp4>(p, it, w1);
-    bool v2 = v1 && pack_next(it, sched, groups);
-    pack_load<fp4>(p, it, w2);
-    int stage = 0;
-    uint32_t phase = 0;
-    while (v0) {
-      if (!warp_wait_bar(ptx::smem_u32(&empty[stage]), phase ^ 1, ctl)) break;
-      uint8_t* xsf = smem + stage * stage_bytes + off_xsf;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t*>(xsf + 16 * lane + 4 * r) = w0[r];
-      if constexpr (fp4) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t*>(xsf + kSfChunk + 16 * lane + 4 * r) = w0[4 + r];
-      }
-      ptx::fence_proxy_async_smem();  // make the generic-proxy stores visible to tcgen05.cp
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&full[stage]));
-      if (++stage == n_stages) {
-        stage = 0;
-        phase ^= 1;
-      }
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        w0[r] = w1[r];
-        w1[r] = w2[r];
-      }
-      v0 = v1;
-      v1 = v2;
-      v2 = v2 && pack_next(it, sched, groups);
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ token-scale packers
+    // Each packer walks the whole (segment, K block) sequence and loads its own items'
+    // scale words three of its items before their stages are filled; it waits about one
+    // L2 round trip per item.  Where that paces the ring (eight words per lane for packed
+    // E2M1) warp 6 fills the even items and warp 7 the odd
+    // ones, running the same code (no instruction-cache cost).  (A 256-thread CTA made the
+    // FP8 path slower on small problems, so FP8 keeps one packer.)
+    constexpr int npk = fp4 ? 2 : 1;
+    const int par = warp - 6;
+    if (par < npk) {
+      PackIter it;
+      it.valid = false;
+      it.e = -1;
+      uint32_t w0[8], w1[8], w2[8];
+      bool v0 = pack_next(it, sched, groups) && (par == 0 || pack_next(it, sched, groups));
+      pack_load<fp4>(p, it, w0);
+      bool v1 = v0 && pack_next(it, sched, groups) && (npk == 1 || pack_next(it, sched, groups));
+      pack_load<fp4>(p, it, w1);
+      bool v2 = v1 && pack_next(it, sched, groups) && (npk == 1 || pack_next(it, sched, groups));
       pack_load<fp4>(p, it, w2);
+      int stage = par;  // item n fills stage n % n_stages (n_stages >= 6)
+      uint32_t phase = 0;
+      while (v0) {
+        if (!warp_wait_bar(ptx::smem_u32(&empty[stage]), phase ^ 1, ctl)) break;
+        uint8_t* xsf = smem + stage * stage_bytes + off_xsf;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t*>(xsf + 16 * lane + 4 * r) = w0[r];
+        if constexpr (fp4) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t*>(xsf + kSfChunk + 16 * lane + 4 * r) = w0[4 + r];
+        }
+        ptx::fence_proxy_async_smem();  // make the generic-proxy stores visible to tcgen05.cp
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&full[stage]));
+        stage += npk;
+        if (stage >= n_stages) {
+          stage -= n_stages;
+          phase ^= 1;
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          w0[r] = w1[r];
+          w1[r] = w2[r];
+        }
+        v0 = v1;
+        v1 = v2;
+        v2 = v2 && pack_next(it, sched, groups) && (npk == 1 || pack_next(it, sched, groups));
+        pack_load<fp4>(p, it, w2);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -738,7 +749,7 @@ cudaError_t launch_gemm(const TokenMaps& tmaps, const GemmParams& p, int grid, c
   // before reading any input
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)grid);
-  lc.blockDim = dim3(kGemmThreads);
+  lc.blockDim = dim3(gemm_threads(p.fp4 != 0));
   lc.dynamicSmemBytes = cfg::kSmemBytes;
   lc.stream = s;
   cudaLaunchAttribute attr[1];
