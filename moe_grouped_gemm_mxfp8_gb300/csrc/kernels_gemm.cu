@@ -526,8 +526,18 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // Shared-memory descriptors of stage 0; stage s adds s * (stage_bytes >> 4) to their
+      // 14-bit start-address field and an MMA's 32-byte K step adds 2 (shared addresses stay
+      // below 2^18, so the field never carries into its neighbours).
+      const uint64_t dA0 = ptx::smem_desc(smem_base, 16, 1024, ptx::kSwizzle128B);                // weight tile
+      const uint64_t dS0 = ptx::smem_desc(smem_base + cfg::kOffWSF, 0, 128, ptx::kSwizzleNone);  // its scales
+      constexpr uint64_t kB = (uint64_t)(cfg::off_x(fp4) >> 4);                          // token rows
+      constexpr uint64_t kXs = (uint64_t)((cfg::off_xsf(fp4) - cfg::kOffWSF) >> 4);      // token scales
+      constexpr uint64_t kHalf = (uint64_t)(kSfChunk >> 4);                               // second scale half
+      const uint32_t dstep = (uint32_t)stage_bytes >> 4;
+      const uint32_t sf0 = tmem_base + 2 * tmax;  // per-stage scale columns follow the accumulators
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, doff = 0, sfoff = 0;
       int acc_i = 0;
       Seg sg;
       bool ok = true;
@@ -548,41 +558,40 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sb = smem_base + stage * stage_bytes;
-          const uint32_t sfa = tmem_base + 2 * tmax + stage * cfg::sf_cols(fp4);  // per-stage scale columns
+          const uint64_t dA = dA0 + doff, dS = dS0 + doff;
+          const uint32_t sfa = sf0 + sfoff;
           if constexpr (fp4) {
-            // two scale chunks per operand (32-blocks 0..3 and 4..7 of the 256-K block); MMA q
-            // covers 32-blocks 2q, 2q + 1: chunk q / 2, bytes 2 (q % 2) and 2 (q % 2) + 1
+            // two scale halves per operand (32-blocks 0..3 and 4..7 of the 256-K block); MMA q
+            // covers 32-blocks 2q, 2q + 1: half q / 2, bytes 2 (q % 2) and 2 (q % 2) + 1
             const uint32_t sfb = sfa + 8;
-            ptx::tc_cp_sf(sfa, ptx::smem_desc(sb + cfg::kOffWSF, 0, 128, ptx::kSwizzleNone));
-            ptx::tc_cp_sf(sfa + 4, ptx::smem_desc(sb + cfg::kOffWSF + kSfChunk, 0, 128, ptx::kSwizzleNone));
-            ptx::tc_cp_sf(sfb, ptx::smem_desc(sb + off_xsf, 0, 128, ptx::kSwizzleNone));
-            ptx::tc_cp_sf(sfb + 4, ptx::smem_desc(sb + off_xsf + kSfChunk, 0, 128, ptx::kSwizzleNone));
+            ptx::tc_cp_sf(sfa, dS);
+            ptx::tc_cp_sf(sfa + 4, dS + kHalf);
+            ptx::tc_cp_sf(sfb, dS + kXs);
+            ptx::tc_cp_sf(sfb + 4, dS + kXs + kHalf);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const uint64_t adesc = ptx::smem_desc(sb + 32 * q, 16, 1024, ptx::kSwizzle128B);
-              const uint64_t bdesc = ptx::smem_desc(sb + off_x + 32 * q, 16, 1024, ptx::kSwizzle128B);
               const uint32_t sid = 2u * (uint32_t)(q & 1);
-              const uint32_t id = idesc | (sid << 4) | (sid << 29);
               const uint32_t col = 4u * (uint32_t)(q >> 1);
-              ptx::tc_mma_mxf4(d_tmem, adesc, bdesc, id, sfa + col, sfb + col, (kb > sg.kb0 || q > 0) ? 1u : 0u);
+              ptx::tc_mma_mxf4(d_tmem, dA + 2 * q, dA + kB + 2 * q, idesc | (sid << 4) | (sid << 29), sfa + col,
+                               sfb + col, (kb > sg.kb0 || q > 0) ? 1u : 0u);
             }
           } else {
             const uint32_t sfb = sfa + 4;
-            ptx::tc_cp_sf(sfa, ptx::smem_desc(sb + cfg::kOffWSF, 0, 128, ptx::kSwizzleNone));
-            ptx::tc_cp_sf(sfb, ptx::smem_desc(sb + off_xsf, 0, 128, ptx::kSwizzleNone));
+            ptx::tc_cp_sf(sfa, dS);
+            ptx::tc_cp_sf(sfb, dS + kXs);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint64_t adesc = ptx::smem_desc(sb + 32 * q, 16, 1024, ptx::kSwizzle128B);
-              const uint64_t bdesc = ptx::smem_desc(sb + off_x + 32 * q, 16, 1024, ptx::kSwizzle128B);
-              const uint32_t id = idesc | ((uint32_t)q << 4) | ((uint32_t)q << 29);
-              ptx::tc_mma_mxf8(d_tmem, adesc, bdesc, id, sfa, sfb, (kb > sg.kb0 || q > 0) ? 1u : 0u);
-            }
+            for (int q = 0; q < 4; ++q)
+              ptx::tc_mma_mxf8(d_tmem, dA + 2 * q, dA + kB + 2 * q, idesc | ((uint32_t)q << 4) | ((uint32_t)q << 29),
+                               sfa, sfb, (kb > sg.kb0 || q > 0) ? 1u : 0u);
           }
           ptx::tc_commit(ptx::smem_u32(&empty[stage]));
+          doff += dstep;
+          sfoff += cfg::sf_cols(fp4);
           if (++stage == n_stages) {
             stage = 0;
             phase ^= 1;
+            doff = 0;
+            sfoff = 0;
           }
         }
         if (!ok) break;
