@@ -527,30 +527,70 @@ def run_ours(args):
         offs[k] = off
         off = (off + inp[k].numel() * inp[k].element_size() + 255) // 256 * 256
     host_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
-    dev_buf = torch.empty(off, dtype=torch.uint8, device="cuda")
-    dev = {}
     for k in names:
         n = inp[k].numel() * inp[k].element_size()
         host_buf[offs[k]:offs[k] + n].copy_(inp[k].contiguous().view(-1).view(torch.uint8))
-        dev[k] = dev_buf[offs[k]:offs[k] + n].view(inp[k].dtype).view(inp[k].shape)
     h2d = off
     out_host = torch.empty_like(inp["out"]).pin_memory()
     d2h = out_host.numel() * out_host.element_size()
+
+    def device_set():
+        buf = torch.empty(off, dtype=torch.uint8, device="cuda")
+        views = dict(d)
+        for k in names:
+            n = inp[k].numel() * inp[k].element_size()
+            views[k] = buf[offs[k]:offs[k] + n].view(inp[k].dtype).view(inp[k].shape)
+        return buf, views
+
+    # (1) serial: each step's copy in, call and copy out one after another, after an L2 flush
+    dev_buf, dd = device_set()
     ee0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ee1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    dd = dict(d)
-    dd.update(dev)
     for i in range(args.warmup + args.steps):
         if i >= args.warmup:
             flush()
             ee0[i - args.warmup].record()
         dev_buf.copy_(host_buf, non_blocking=True)
-        B.run(prob, dd, dev["out"], prepared=prep, ws=ws)
-        out_host.copy_(dev["out"], non_blocking=True)
+        B.run(prob, dd, dd["out"], prepared=prep, ws=ws)
+        out_host.copy_(dd["out"], non_blocking=True)
         if i >= args.warmup:
             ee1[i - args.warmup].record()
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ee0, ee1))
+    e2e_serial_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ee0, ee1))
+
+    # (2) pipelined, as a serving loop runs: two device input sets; step i's copy in (copy
+    # stream) overlaps step i-1's call (compute stream), and its copy out (return stream)
+    # overlaps step i+1.  Every step still copies all its inputs in and its result out.  No
+    # flush between steps (the weights are larger than L2).
+    sets = [(dev_buf, dd), device_set()]
+    s_in, s_main, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    n_all = args.warmup + args.steps
+    ev_in = [torch.cuda.Event() for _ in range(n_all)]
+    ev_call = [torch.cuda.Event() for _ in range(n_all)]
+    ev_out = [torch.cuda.Event() for _ in range(n_all)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    for i in range(n_all):
+        buf, views = sets[i % 2]
+        if i == args.warmup:  # the timed steps start with the warm-up steps drained
+            if i > 0:
+                s_in.wait_event(ev_out[i - 1])
+            t_start.record(s_in)
+        if i >= 2:
+            s_in.wait_event(ev_out[i - 2])  # the set's previous result has been read back
+        with torch.cuda.stream(s_in):
+            buf.copy_(host_buf, non_blocking=True)
+        ev_in[i].record(s_in)
+        s_main.wait_event(ev_in[i])
+        B.run(prob, views, views["out"], prepared=prep, ws=ws, stream=s_main)
+        ev_call[i].record(s_main)
+        s_out.wait_event(ev_call[i])
+        with torch.cuda.stream(s_out):
+            out_host.copy_(views["out"], non_blocking=True)
+        ev_out[i].record(s_out)
+    t_end.record(s_out)
+    torch.cuda.synchronize()
+    e2e_ms = t_start.elapsed_time(t_end) / args.steps
 
     peaks, peak_kind = _peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -573,8 +613,11 @@ def run_ours(args):
                      "frac": gemm_gbs / hbm_peak, "traffic": _profiled_traffic(spec.name),
                      "kernel": "gemm_kernel (grouped GEMM + fused epilogue)",
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
-        "e2e": {"value": alg_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "e2e": {"value": alg_bytes / (e2e_serial_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_serial_ms,
+                "mode": "serial: each step's copy in, call and copy out back to back, L2 flushed before",
+                "pipelined_value": alg_bytes / (e2e_ms * 1e-3) / 1e9 * world, "pipelined_ms_per_step": e2e_ms,
+                "pipelined_mode": "copy in, call and copy out of consecutive steps overlap on three streams"},
         "gpu_launches": args.steps * (3 if args.deterministic else 1),
         "device_error_bits": bits,
         "clocks": clk.summary(),
