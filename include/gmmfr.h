@@ -307,9 +307,10 @@ GMMFR_API const char* gmmfr_last_error(void);
  * ms[call * GMMFR_PROFILE_SLOTS + slot] (-1 where a slot's kernel did not run),
  * sets *n_calls, and stops recording.
  * Slots: 0 input preparation inside the call (weight preparation when no prepared
- * weights are given, E2M1 token expansion), 1 deterministic-mode routing (row
- * CSR of the tokens), 2 grouped GEMM with fused epilogue, 3 deterministic combine,
- * 4 the whole call (start of its first kernel to end of its last).
+ * weights are given, E2M1 token expansion), 1 not used (the deterministic mode's
+ * row CSR of the tokens is built inside the grouped GEMM), 2 grouped GEMM with fused
+ * epilogue, 3 deterministic combine, 4 the whole call (start of its first kernel to
+ * end of its last).
  */
 #define GMMFR_PROFILE_SLOTS 5
 GMMFR_API gmmfr_status gmmfr_profile_begin(int max_calls);

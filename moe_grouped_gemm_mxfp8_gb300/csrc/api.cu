@@ -1,6 +1,6 @@
 // C ABI of the MXFP8 grouped-matmul-finalize-routing library (declared in
 // include/gmmfr.h): argument checks, workspace layout, tensor map of x1, and the
-// launch sequence (deterministic routing ->) grouped GEMM (-> deterministic combine).
+// launch sequence: grouped GEMM (-> deterministic combine).
 #include "gmmfr.h"
 
 #include <cudaTypedefs.h>
@@ -308,26 +308,10 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
     }
   }
 
+  // deterministic mode: the row CSR of the tokens lives in the workspace; the GEMM kernel
+  // builds it and the combine kernel walks it
   int32_t* row_ptr = det ? reinterpret_cast<int32_t*>(ws + L.off_rowptr) : nullptr;
   int32_t* sorted = det ? reinterpret_cast<int32_t*>(ws + L.off_sorted) : nullptr;
-  if (det) {
-    gmmfr::CsrParams rp{};
-    rp.group_list = group_list;
-    rp.row_index = row_index;
-    rp.cnt = reinterpret_cast<int32_t*>(ws + L.off_cnt);
-    rp.row_ptr = row_ptr;
-    rp.cursor = reinterpret_cast<int32_t*>(ws + L.off_cursor);
-    rp.sorted = sorted;
-    rp.M = p.M;
-    rp.batch = p.batch;
-    rp.E = (int32_t)p.E;
-    rp.group_list_type = p.group_list_type;
-    rp.row_i32 = p.row_index_type == GMMFR_INDEX_I32;
-    timer.begin(1, s);
-    e = gmmfr::launch_row_csr(rp, s);
-    timer.end(1, s);
-    if (e != cudaSuccess) return cuda_fail(e, "routing launch");
-  }
 
   gmmfr::GemmParams gp{};
   gp.prepared = wprep;
@@ -340,6 +324,10 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   gp.bias = static_cast<const uint16_t*>(bias);
   gp.out = out;
   gp.ybuf = det ? reinterpret_cast<float*>(ws + L.off_y) : nullptr;
+  gp.csr_cnt = det ? reinterpret_cast<int32_t*>(ws + L.off_cnt) : nullptr;
+  gp.csr_row_ptr = row_ptr;
+  gp.csr_cursor = det ? reinterpret_cast<int32_t*>(ws + L.off_cursor) : nullptr;
+  gp.csr_sorted = sorted;
   gp.M = p.M;
   gp.N = p.N;
   gp.K = p.K;

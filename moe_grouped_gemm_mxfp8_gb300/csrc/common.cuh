@@ -47,20 +47,6 @@ struct PrepParams {
 };
 cudaError_t launch_expand_fp4(const uint8_t* packed, uint8_t* fp8, int64_t n_bytes, cudaStream_t s);
 
-// Deterministic mode: tokens of each out row (CSR, unordered within a row).
-struct CsrParams {
-  const int64_t* group_list;
-  const void* row_index;
-  int32_t* cnt;
-  int32_t* row_ptr;
-  int32_t* cursor;
-  int32_t* sorted;
-  int64_t M, batch;
-  int32_t E;
-  int32_t group_list_type;
-  int32_t row_i32;
-};
-
 struct GemmParams {
   const uint8_t* prepared;
   const int64_t* group_list;
@@ -71,6 +57,11 @@ struct GemmParams {
   const uint16_t* bias;    // [E, N] bf16 bits or null
   float* out;
   float* ybuf;             // deterministic: [split][M][N]
+  // deterministic: tokens of each out row (CSR, unordered within a row), built by CTA 0
+  int32_t* csr_cnt;        // [batch] counts
+  int32_t* csr_row_ptr;    // [batch + 1]
+  int32_t* csr_cursor;     // [batch] scatter cursors
+  int32_t* csr_sorted;     // [M] token indices grouped by row
   uint32_t* hdr;           // error slots (see kHdrBytes)
   int64_t M, N, K, batch;
   int64_t shared_rows, shared_offset;
@@ -148,7 +139,6 @@ cudaError_t launch_ffn_gemm(const TokenMaps& tmaps, const FfnParams& p, int grid
 
 // launchers (defined next to their kernels)
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
-cudaError_t launch_row_csr(const CsrParams& p, cudaStream_t s);
 // x1 [M, K] as 2-D tensors of 128-byte rows, boxes of 16, 32, 64 and 128 rows (128-byte swizzle).
 struct TokenMaps {
   CUtensorMap m[4];

@@ -1,9 +1,10 @@
 // Auxiliary kernels of MXFP8 grouped-matmul-finalize-routing:
 //   - E2M1 (MXFP4) token expansion to E4M3,
 //   - weight preparation (one-time re-layout of x2 and its scales into GEMM tiles),
-//   - deterministic-mode routing (row CSR of the routed tokens),
-//   - deterministic combine (row-ordered sum of the per-token results).
+//   - deterministic combine (row-ordered sum of the per-token results; the row CSR
+//     of the routed tokens it walks is built inside the grouped GEMM kernel).
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace gmmfr {
 
@@ -219,96 +220,6 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// ============================================================================ prologue
-// Block-wide inclusive scan over 1024 threads (sum or max) of int64 values.
-// `total` receives the scan's last value.
-template <bool kMax>
-__device__ int64_t block_scan_incl(int64_t v, int64_t* s_warp, int64_t* total = nullptr) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v = kMax ? (u > v ? u : v) : v + u;
-  }
-  if (lane == 31) s_warp[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    int64_t w = s_warp[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t u = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w = kMax ? (u > w ? u : w) : w + u;
-    }
-    s_warp[lane] = w;
-  }
-  __syncthreads();
-  if (warp > 0) {
-    const int64_t u = s_warp[warp - 1];
-    v = kMax ? (u > v ? u : v) : v + u;
-  }
-  if (total) *total = s_warp[31];
-  __syncthreads();
-  return v;
-}
-
-__device__ __forceinline__ int64_t load_row(const void* rows, int row_i32, int64_t t) {
-  return row_i32 ? (int64_t) static_cast<const int32_t*>(rows)[t] : static_cast<const int64_t*>(rows)[t];
-}
-
-// Deterministic mode: one block of 1024 threads decodes the expert ranges (as
-// the GEMM kernel does: contiguous, clamped to [0, M]) to find the covered
-// tokens [0, covered), then builds the CSR of covered tokens by out row.
-// Positions within a row come from atomics; the combine kernel orders them.
-__global__ void __launch_bounds__(1024) row_csr_kernel(CsrParams p) {
-  __shared__ int64_t s_warp[32];
-  __shared__ int64_t s_covered;
-  const int tid = threadIdx.x;
-  const int64_t M = p.M;
-  const int64_t g = tid < p.E ? p.group_list[tid] : 0;
-  int64_t end;
-  if (p.group_list_type == 1) {
-    const int64_t c = tid < p.E ? (g < 0 ? 0 : (g > M ? M + 1 : g)) : 0;
-    const int64_t incl = block_scan_incl<false>(c, s_warp);
-    end = incl < M ? incl : M;
-  } else {
-    const int64_t c = tid < p.E ? (g < 0 ? 0 : (g > M ? M : g)) : 0;
-    const int64_t incl = block_scan_incl<true>(c, s_warp);
-    end = incl < M ? incl : M;
-  }
-  if (tid == p.E - 1) s_covered = end;
-  for (int64_t r = tid; r < p.batch; r += blockDim.x) p.cnt[r] = 0;
-  __syncthreads();
-  const int64_t covered = s_covered;
-  for (int64_t t = tid; t < covered; t += blockDim.x) {
-    const int64_t r = load_row(p.row_index, p.row_i32, t);
-    if (r >= 0 && r < p.batch) atomicAdd(&p.cnt[r], 1);
-  }
-  __syncthreads();
-  int64_t running = 0;
-  for (int64_t base = 0; base < p.batch; base += blockDim.x) {
-    const int64_t r = base + tid;
-    const int64_t c = r < p.batch ? p.cnt[r] : 0;
-    int64_t chunk_total = 0;
-    const int64_t incl = block_scan_incl<false>(c, s_warp, &chunk_total);
-    if (r < p.batch) {
-      p.row_ptr[r] = (int32_t)(running + incl - c);
-      p.cursor[r] = (int32_t)(running + incl - c);
-    }
-    running += chunk_total;
-  }
-  if (tid == 0) p.row_ptr[p.batch] = (int32_t)running;
-  __syncthreads();
-  for (int64_t t = tid; t < covered; t += blockDim.x) {
-    const int64_t r = load_row(p.row_index, p.row_i32, t);
-    if (r >= 0 && r < p.batch) p.sorted[atomicAdd(&p.cursor[r], 1)] = (int32_t)t;
-  }
-}
-
-cudaError_t launch_row_csr(const CsrParams& p, cudaStream_t s) {
-  row_csr_kernel<<<1, 1024, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
 // ============================================================================ deterministic combine
 constexpr int kCombineThreads = 256;
 constexpr int kCombineCap = 2048;  // row segments up to this length are ordered in shared memory
@@ -321,6 +232,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
   __shared__ int32_t s_tok[kCombineCap];
   __shared__ int32_t s_ord[kCombineCap];
   __shared__ int32_t s_min[kCombineThreads / 32];
+  // launched as a programmatic dependent of the grouped GEMM: Y and the row CSR are read only
+  // after that kernel has completed
+  ptx::griddep_wait();
   const int64_t r = blockIdx.x;
   const int tid = threadIdx.x;
   const int beg = p.row_ptr[r];
@@ -384,9 +298,18 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   if (p.batch == 0 || p.N == 0) return cudaSuccess;
   const int64_t cols = (p.N + 4 * kCombineThreads - 1) / (4 * kCombineThreads);
-  dim3 grid((unsigned)p.batch, (unsigned)cols);
-  combine_kernel<<<grid, kCombineThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  // programmatic stream serialization: the launch overlaps the GEMM's tail (the GEMM lets it
+  // start early); the kernel waits for the GEMM before reading anything
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)p.batch, (unsigned)cols);
+  lc.blockDim = dim3(kCombineThreads);
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, combine_kernel, p);
 }
 
 }  // namespace gmmfr

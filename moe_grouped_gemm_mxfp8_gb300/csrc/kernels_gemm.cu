@@ -204,9 +204,11 @@ struct Sched {
     cur_g = (int)(tile % (ng > 0 ? ng : 1));
     cur_j = (int)(tile / (ng > 0 ? ng : 1));
   }
-  __device__ bool next(Seg& s) {
+  // kDet: the kernel's mode (compile time, so each instantiation holds one walk)
+  template <bool kDet>
+  __device__ __forceinline__ bool next(Seg& s) {
     if (i >= i_end) return false;
-    if (!det) {  // tiles in order j * n_groups + g; a segment runs to its tile's end or the range's
+    if constexpr (!kDet) {  // tiles in order j * n_groups + g; a segment runs to its tile's end or the range's
       s.g = cur_g;
       s.j = cur_j;
       s.kb0 = cur_kb;
@@ -220,16 +222,17 @@ struct Sched {
         ++cur_j;
       }
       return true;
+    } else {  // deterministic: (group, tile, K split) units round-robin over the CTAs
+      const int64_t tile = i / split;
+      const int sp = (int)(i % split);
+      s.kb0 = (int)((int64_t)sp * KB / split);
+      s.kb1 = (int)((int64_t)(sp + 1) * KB / split);
+      s.slot = sp;
+      i += step;
+      s.g = (int)(tile % ng);
+      s.j = (int)(tile / ng);
+      return true;
     }
-    const int64_t tile = i / split;
-    const int sp = (int)(i % split);
-    s.kb0 = (int)((int64_t)sp * KB / split);
-    s.kb1 = (int)((int64_t)(sp + 1) * KB / split);
-    s.slot = sp;
-    i += step;
-    s.g = (int)(tile % ng);
-    s.j = (int)(tile / ng);
-    return true;
   }
 };
 
@@ -339,6 +342,57 @@ __device__ void shared_add_slice(const GemmParams& p, int ep_tid) {
   }
 }
 
+// Deterministic mode: the tokens of each out row (CSR, unordered within a row; the combine
+// orders them), from the covered tokens [0, covered) of the decoded expert ranges.  Built by
+// the 128 epilogue threads of one CTA (named barrier 1) before its first tile, in time those
+// warps spend waiting anyway; the combine kernel reads it after this kernel has completed.
+__device__ void build_row_csr(const GemmParams& p, int64_t covered, int ep_tid, int64_t* scratch) {
+  const int lane = ep_tid & 31, w = ep_tid >> 5;
+  for (int64_t r = ep_tid; r < p.batch; r += 128) p.csr_cnt[r] = 0;
+  __threadfence_block();
+  ptx::bar_sync(1, 128);
+  for (int64_t t = ep_tid; t < covered; t += 128) {
+    const int r = load_row32(p.row_index, p.row_i32, t, p.batch);
+    if (r >= 0) atomicAdd(&p.csr_cnt[r], 1);
+  }
+  __threadfence_block();
+  ptx::bar_sync(1, 128);
+  int64_t running = 0;  // exclusive scan of the counts, 128 rows at a time
+  for (int64_t base = 0; base < p.batch; base += 128) {
+    const int64_t r = base + ep_tid;
+    const int c = r < p.batch ? __ldcg(&p.csr_cnt[r]) : 0;  // counts were made by atomics (L2)
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) scratch[w] = incl;
+    ptx::bar_sync(1, 128);
+    int64_t before = 0, chunk = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t v = scratch[k];
+      before += k < w ? v : 0;
+      chunk += v;
+    }
+    if (r < p.batch) {
+      const int32_t start = (int32_t)(running + before + incl - c);
+      p.csr_row_ptr[r] = start;
+      p.csr_cursor[r] = start;
+    }
+    running += chunk;
+    ptx::bar_sync(1, 128);  // scratch is rewritten by the next chunk
+  }
+  if (ep_tid == 0) p.csr_row_ptr[p.batch] = (int32_t)running;
+  __threadfence_block();
+  ptx::bar_sync(1, 128);
+  for (int64_t t = ep_tid; t < covered; t += 128) {
+    const int r = load_row32(p.row_index, p.row_i32, t, p.batch);
+    if (r >= 0) p.csr_sorted[atomicAdd(&p.csr_cursor[r], 1)] = (int32_t)t;
+  }
+}
+
 // The four E8M0 bytes of token t for the 32-element blocks 4*c .. 4*c+3 (c = kb for FP8
 // blocks, 2*kb and 2*kb + 1 for the two halves of a packed E2M1 block); blocks starting at
 // or past K are padding: 127 = 1.0.
@@ -362,9 +416,10 @@ struct PackIter {
   bool valid;
 };
 
+template <bool kDet>
 __device__ __forceinline__ bool pack_next(PackIter& it, Sched& sched, const Groups& groups) {
   if (it.valid && ++it.kb < it.kb1) return true;
-  while (sched.next(it.sg)) {
+  while (sched.next<kDet>(it.sg)) {
     groups.info(it.sg.g, it.e, it.t0, it.T);
     it.kb = it.sg.kb0;
     it.kb1 = it.sg.kb1;
@@ -392,9 +447,10 @@ __device__ __forceinline__ void pack_load(const GemmParams& p, const PackIter& i
   }
 }
 
-// fp4: packed E2M1 operands (kind::mxf4); a separate instantiation keeps each format's
-// loops free of the other's code.
-template <bool fp4>
+// fp4: packed E2M1 operands (kind::mxf4); det: deterministic mode.  Separate instantiations
+// keep each variant's loops free of the others' code (the instruction cache is the scarce
+// resource: one in five fetches misses it).
+template <bool fp4, bool det>
 __global__ void __launch_bounds__(gemm_threads(fp4), 1)
     gemm_kernel(const __grid_constant__ TokenMaps tmaps, const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -419,6 +475,8 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
   // launched as a programmatic dependent of the kernel before it (the routing step): every
   // input may be that kernel's output, so nothing is read before it has completed
   ptx::griddep_wait();
+  // deterministic mode: the combine kernel that follows may launch now (it waits for this grid)
+  if constexpr (det) ptx::griddep_launch_dependents();
   const int64_t g0 = threadIdx.x < p.E ? p.group_list[threadIdx.x] : 0;
 
   if (threadIdx.x == 0) {
@@ -455,7 +513,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
   const int off_xsf = cfg::off_xsf(fp4), off_x = cfg::off_x(fp4);
   const Ctl ctl{abort_flag, s_err, p.timeout_ns};
   Sched sched;
-  sched.init(n_groups, p.NT, p.KB, p.deterministic != 0, p.split, groups);
+  sched.init(n_groups, p.NT, p.KB, det, p.split, groups);
   const uint32_t smem_base = ptx::smem_u32(smem);
 
   if (warp == 0) {
@@ -473,7 +531,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       if (p.test_stall) ok = wait_bar(ptx::smem_u32(stall), 0, ctl);
       Seg sg;
       int e = -1;
-      while (ok && sched.next(sg)) {
+      while (ok && sched.next<det>(sg)) {
         int t0, T;
         groups.info(sg.g, e, t0, T);
         const int m = (T + 15) / 16;  // token rows in 16-row units: boxes of 128/64/32/16 rows
@@ -542,7 +600,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       Seg sg;
       bool ok = true;
       int e = -1;
-      while (ok && sched.next(sg)) {
+      while (ok && sched.next<det>(sg)) {
         int t0, T;
         groups.info(sg.g, e, t0, T);
         const uint32_t npad = (uint32_t)((T + 15) / 16) * 16;
@@ -622,11 +680,11 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       it.valid = false;
       it.e = -1;
       uint32_t w0[8], w1[8], w2[8];
-      bool v0 = pack_next(it, sched, groups) && (par == 0 || pack_next(it, sched, groups));
+      bool v0 = pack_next<det>(it, sched, groups) && (par == 0 || pack_next<det>(it, sched, groups));
       pack_load<fp4>(p, it, w0);
-      bool v1 = v0 && pack_next(it, sched, groups) && (npk == 1 || pack_next(it, sched, groups));
+      bool v1 = v0 && pack_next<det>(it, sched, groups) && (npk == 1 || pack_next<det>(it, sched, groups));
       pack_load<fp4>(p, it, w1);
-      bool v2 = v1 && pack_next(it, sched, groups) && (npk == 1 || pack_next(it, sched, groups));
+      bool v2 = v1 && pack_next<det>(it, sched, groups) && (npk == 1 || pack_next<det>(it, sched, groups));
       pack_load<fp4>(p, it, w2);
       int stage = par;  // item n fills stage n % n_stages (n_stages >= 6)
       uint32_t phase = 0;
@@ -654,7 +712,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
         }
         v0 = v1;
         v1 = v2;
-        v2 = v2 && pack_next(it, sched, groups) && (npk == 1 || pack_next(it, sched, groups));
+        v2 = v2 && pack_next<det>(it, sched, groups) && (npk == 1 || pack_next<det>(it, sched, groups));
         pack_load<fp4>(p, it, w2);
       }
     }
@@ -664,12 +722,15 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
     const int ep_tid = threadIdx.x - 64;
     // the shared add (atomic mode) runs after the first tile's epilogue, in time the epilogue
     // warps spend waiting anyway; at kernel entry its atomics delayed the first weight loads
-    bool shared_pending = !p.deterministic && p.shared != nullptr && p.shared_rows > 0 && p.N > 0;
+    bool shared_pending = !det && p.shared != nullptr && p.shared_rows > 0 && p.N > 0;
+    if constexpr (det) {
+      if (blockIdx.x == 0) build_row_csr(p, s_end[p.E - 1], ep_tid, s_scan);
+    }
     int acc_i = 0;
     Seg sg;
     bool bad_row = false;
     int e = -1;
-    while (sched.next(sg)) {
+    while (sched.next<det>(sg)) {
       int t0, T;
       groups.info(sg.g, e, t0, T);
       const int buf = acc_i & 1;
@@ -701,7 +762,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
         const int cnt = T - c0 < 32 ? T - c0 : 32;
         // one unrolled loop per mode, so the atomic mode's hot code holds no store path of
         // the deterministic one (the instruction cache is the scarce resource here)
-        if (p.deterministic) {
+        if constexpr (det) {
           float* y = p.ybuf + ((int64_t)sg.slot * p.M + t0 + c0) * p.N + n;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
@@ -751,9 +812,9 @@ cudaError_t launch_gemm(const TokenMaps& tmaps, const GemmParams& p, int grid, c
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg::kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg::kSmemBytes);
+    cudaError_t e = cudaSuccess;
+    for (auto k : {gemm_kernel<false, false>, gemm_kernel<false, true>, gemm_kernel<true, false>, gemm_kernel<true, true>})
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
@@ -770,7 +831,9 @@ cudaError_t launch_gemm(const TokenMaps& tmaps, const GemmParams& p, int grid, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return p.fp4 ? cudaLaunchKernelEx(&lc, gemm_kernel<true>, tmaps, p) : cudaLaunchKernelEx(&lc, gemm_kernel<false>, tmaps, p);
+  auto kernel = p.fp4 ? (p.deterministic ? gemm_kernel<true, true> : gemm_kernel<true, false>)
+                     : (p.deterministic ? gemm_kernel<false, true> : gemm_kernel<false, false>);
+  return cudaLaunchKernelEx(&lc, kernel, tmaps, p);
 }
 
 }  // namespace gmmfr
