@@ -197,6 +197,9 @@ __device__ __forceinline__ bool epi_all(bool ok) {  // vote over the 4 epilogue 
 
 }  // namespace
 
+// kGateUp: GEMM1 with the SwiGLU epilogue (p.gate_up); a separate instantiation per GEMM keeps
+// each launch's code to its own epilogue.
+template <bool kGateUp>
 __global__ void __launch_bounds__(ffn::kThreads, 1)
     ffn_gemm_kernel(const __grid_constant__ TokenMaps tmaps, const __grid_constant__ FfnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
   int* abort_flag = &misc[1];
   uint32_t* s_err = reinterpret_cast<uint32_t*>(&misc[2]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (p.gate_up) ptx::griddep_launch_dependents();  // GEMM2 may launch (it waits for GEMM1 before reading sw)
+  if constexpr (kGateUp) ptx::griddep_launch_dependents();  // GEMM2 may launch (it waits for GEMM1 before reading sw)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ffn::kMaxStages; ++s) {
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
           if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acce[buf]));
         }
         const int cnt = T - c0 < 32 ? T - c0 : 32;
-        if (p.gate_up) {
+        if constexpr (kGateUp) {
           // lanes of quadrants 2, 3 hold the up columns matching quadrants 0, 1
           if (q >= 2) {
 #pragma unroll
@@ -469,12 +472,15 @@ cudaError_t launch_ffn_gemm(const TokenMaps& tmaps, const FfnParams& p, int grid
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ffn::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(ffn_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ffn::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ffn_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ffn::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
+  auto kernel = p.gate_up ? ffn_gemm_kernel<true> : ffn_gemm_kernel<false>;
   if (!p.dependent) {
-    ffn_gemm_kernel<<<grid, ffn::kThreads, ffn::kSmemBytes, s>>>(tmaps, p);
+    kernel<<<grid, ffn::kThreads, ffn::kSmemBytes, s>>>(tmaps, p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t lc = {};  // programmatic dependent of the previous kernel (GEMM1)
@@ -487,7 +493,7 @@ cudaError_t launch_ffn_gemm(const TokenMaps& tmaps, const FfnParams& p, int grid
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, ffn_gemm_kernel, tmaps, p);
+  return cudaLaunchKernelEx(&lc, kernel, tmaps, p);
 }
 
 }  // namespace gmmfr
