@@ -512,8 +512,6 @@ def run_ours(args):
     prof_ms, _, _ = timed_steps(args.steps, False)
     kernel_ms = B.gmmfr_profile_end(args.steps)
     gemm_ms = statistics.mean(k[2] for k in kernel_ms)
-    route = [k[1] for k in kernel_ms if k[1] >= 0]
-    pro_ms = statistics.mean(route) if route else None
     comb = [k[3] for k in kernel_ms if k[3] >= 0]
     comb_ms = statistics.mean(comb) if comb else None
 
@@ -606,7 +604,7 @@ def run_ours(args):
         "us_per_call_p10_p50_p90": [round(float(x) * 1e3, 2) for x in _quantiles(call_ms, (0.1, 0.5, 0.9))],
         "us_per_call_profiled": statistics.mean(k[4] for k in kernel_ms) * 1e3, "tflops": flops / (ms * 1e-3) / 1e12,
         "roofline_fraction_call": gbs / world / hbm_peak,
-        "kernels_ms": {"route": pro_ms, "gemm": gemm_ms, "combine": comb_ms},
+        "kernels_ms": {"gemm": gemm_ms, "combine": comb_ms},
         "weight_prep_ms": prep_ms,
         "weight_prep_gbs": 2 * n_prep / (prep_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": gemm_gbs, "peak": hbm_peak, "unit": "GB/s",
