@@ -33,8 +33,8 @@
 // groups of 64 or 128 are in play, of equal cost (item_cost: CTAs holding 128-token
 // groups get fewer items than those holding 16-token ones); a tile cut between CTAs is finished by
 // atomics, which is exact up to FP32 rounding order since every term is linear.
-// Deterministic mode gives each (group, tile, K-split) unit to one CTA and
-// stores its result for the row-ordered combine.
+// Deterministic mode gives each (group, tile, K-split) unit to one CTA (contiguous
+// ranges of units) and stores its result for the row-ordered combine.
 //
 // Every wait is bounded: on timeout the CTA sets GMMFR_DEV_TIMEOUT, stops
 // issuing, waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
@@ -168,7 +168,7 @@ struct Sched {
   int64_t i, i_end, step;
   int NT, KB, split, ng;
   bool det;
-  int cur_g, cur_j, cur_kb;  // atomic mode: group, column tile and K block of item i
+  int cur_g, cur_j, cur_kb;  // group, column tile and K block of item i (deterministic: K split)
   __device__ void init(int n_groups, int NT_, int KB_, bool det_, int split_, const Groups& gr) {
     ng = n_groups;
     NT = NT_;
@@ -177,9 +177,16 @@ struct Sched {
     split = split_;
     const int64_t tiles = (int64_t)n_groups * NT;
     if (det) {
-      i = blockIdx.x;
-      i_end = tiles * split;
-      step = gridDim.x;
+      // contiguous ranges of (group, tile, K split) units: unit u = tile * split + sp, walked
+      // from the first without dividing (cur_kb holds sp)
+      const int64_t units = tiles * split;
+      i = units * blockIdx.x / gridDim.x;
+      i_end = units * (blockIdx.x + 1) / gridDim.x;
+      step = 1;
+      const int64_t tile = i / split;
+      cur_kb = (int)(i - tile * split);
+      cur_g = (int)(tile % (ng > 0 ? ng : 1));
+      cur_j = (int)(tile / (ng > 0 ? ng : 1));
       return;
     }
     step = 0;
@@ -222,15 +229,21 @@ struct Sched {
         ++cur_j;
       }
       return true;
-    } else {  // deterministic: (group, tile, K split) units round-robin over the CTAs
-      const int64_t tile = i / split;
-      const int sp = (int)(i % split);
+    } else {  // deterministic: the next (group, tile, K split) unit of this CTA's range
+      const int sp = cur_kb;
+      s.g = cur_g;
+      s.j = cur_j;
       s.kb0 = (int)((int64_t)sp * KB / split);
       s.kb1 = (int)((int64_t)(sp + 1) * KB / split);
       s.slot = sp;
-      i += step;
-      s.g = (int)(tile % ng);
-      s.j = (int)(tile / ng);
+      ++i;
+      if (++cur_kb == split) {
+        cur_kb = 0;
+        if (++cur_g == ng) {
+          cur_g = 0;
+          ++cur_j;
+        }
+      }
       return true;
     }
   }
