@@ -266,9 +266,7 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_stream = ptx::l2_evict_first_policy();
       const uint64_t pol_keep = ptx::l2_evict_last_policy();
-      int fills[ffn::kMaxStages];
-#pragma unroll
-      for (int s = 0; s < ffn::kMaxStages; ++s) fills[s] = 0;
+      int64_t n_fill = 0;  // stages filled; stage s was filled n_fill / n_stages (+1 if s < n_fill % n_stages) times
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -330,7 +328,7 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
             pend_m[np] = m;
             if (++np == n_stages) release_pending();  // every stage is in use: the ring needs the tokens
           }
-          ++fills[stage];
+          ++n_fill;
           if (++stage == n_stages) {
             stage = 0;
             phase ^= 1;
@@ -347,12 +345,16 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
         }
       }
       if (ok) {
-        for (int s = 0; s < n_stages; ++s)
-          if (fills[s] > 0 && !wait_bar(ptx::smem_u32(&empty[s]), (fills[s] - 1) & 1, ctl)) break;
+        for (int s = 0; s < n_stages; ++s) {
+          const int64_t fs = n_fill / n_stages + (s < n_fill % n_stages ? 1 : 0);
+          if (fs > 0 && !wait_bar(ptx::smem_u32(&empty[s]), (uint32_t)((fs - 1) & 1), ctl)) break;
+        }
       }
       if (*abort_flag) {
-        for (int s = 0; s < n_stages; ++s)
-          if (fills[s] > 0) wait_bar_drain(ptx::smem_u32(&full[s]), (fills[s] - 1) & 1);
+        for (int s = 0; s < n_stages; ++s) {
+          const int64_t fs = n_fill / n_stages + (s < n_fill % n_stages ? 1 : 0);
+          if (fs > 0) wait_bar_drain(ptx::smem_u32(&full[s]), (uint32_t)((fs - 1) & 1));
+        }
       }
     }
     __syncwarp();

@@ -535,9 +535,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       const uint64_t pol_stream = ptx::l2_evict_first_policy();  // weights read once
       const uint64_t pol_keep = ptx::l2_evict_last_policy();     // tokens (reused by every column tile), and
                                                                  // weights of experts spanning several groups
-      int fills[cfg::kMaxStages];
-#pragma unroll
-      for (int s = 0; s < cfg::kMaxStages; ++s) fills[s] = 0;
+      int64_t n_fill = 0;  // stages filled; stage s was filled n_fill / n_stages (+1 if s < n_fill % n_stages) times
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -577,7 +575,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
             ptx::tma_load_2d(sb + off_x + row * 128, &tmaps.m[last16 ? 0 : 1], kb * kTileK, t0 + row, fb,
                              pol_keep);
           }
-          ++fills[stage];
+          ++n_fill;
           if (++stage == n_stages) {
             stage = 0;
             phase ^= 1;
@@ -585,12 +583,16 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
         }
       }
       if (ok) {  // all fills consumed: wait until the MMA warp has released every stage
-        for (int s = 0; s < n_stages; ++s)
-          if (fills[s] > 0 && !wait_bar(ptx::smem_u32(&empty[s]), (fills[s] - 1) & 1, ctl)) break;
+        for (int s = 0; s < n_stages; ++s) {
+          const int64_t fs = n_fill / n_stages + (s < n_fill % n_stages ? 1 : 0);
+          if (fs > 0 && !wait_bar(ptx::smem_u32(&empty[s]), (uint32_t)((fs - 1) & 1), ctl)) break;
+        }
       }
       if (*abort_flag) {  // aborted: let every issued copy land before shared memory is released
-        for (int s = 0; s < n_stages; ++s)
-          if (fills[s] > 0) wait_bar_drain(ptx::smem_u32(&full[s]), (fills[s] - 1) & 1);
+        for (int s = 0; s < n_stages; ++s) {
+          const int64_t fs = n_fill / n_stages + (s < n_fill % n_stages ? 1 : 0);
+          if (fs > 0) wait_bar_drain(ptx::smem_u32(&full[s]), (uint32_t)((fs - 1) & 1));
+        }
       }
     }
     __syncwarp();
