@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(RouteScatterParams p
   scatter_entry(p, f, (int64_t)p.tile_counts[(f / kRouteTile) * (p.E + 1) + key] + p.rank[f], lane);
 }
 
-__global__ void __launch_bounds__(kFuseThreads, 4) route_fused_kernel(RouteScatterParams p) {
+__global__ void __launch_bounds__(kFuseThreads, 3) route_fused_kernel(RouteScatterParams p) {
   __shared__ int32_t s_key[kFuseMaxM];
   __shared__ int32_t s_cnt[kMaxExperts + 1];   // entries per key
   __shared__ int32_t s_base[kMaxExperts + 1];  // first output position of each key
@@ -268,7 +268,7 @@ cudaError_t launch_route_kernels(const RouteScatterParams& p, cudaStream_t s) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     int64_t grid = (p.M + 7) / 8;  // about one entry per warp
-    if (grid > 4 * sms) grid = 4 * sms;
+    if (grid > 3 * sms) grid = 3 * sms;  // one wave: three CTAs per SM (77 registers, no spills)
     const int64_t min_grid = (p.M + kFuseMaxSlice - 1) / kFuseMaxSlice;  // every slice fits s_pos
     if (grid < min_grid) grid = min_grid;
     if (grid < 1) grid = 1;
