@@ -92,7 +92,8 @@ constexpr int kWbaseOff = kGbaseOff + 4 * (kMaxExperts + 4); // int32 s_wbase[10
 constexpr int kScanOff = kWbaseOff + 4 * (kMaxExperts + 4);  // int64 scan scratch[8]
 static_assert(gemm_threads(true) <= 8 * 32 && gemm_threads(false) <= 8 * 32, "scan scratch: one word per warp");
 constexpr int kMiscOff = kScanOff + 8 * 8;                   // int32 misc[8]
-constexpr int kSmemBytes = kMiscOff + 32 + 1024;             // + alignment slack
+constexpr int kTokOff = kMiscOff + 32;                       // int32 rows[2][128], float logits[2][128]
+constexpr int kSmemBytes = kTokOff + 2 * 2 * 128 * 4 + 1024; // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 }  // namespace cfg
 
@@ -741,6 +742,9 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
     if constexpr (det) {
       if (blockIdx.x == 0) build_row_csr(p, s_end[p.E - 1], ep_tid, s_scan);
     }
+    // the tile's token rows and logits, [2][128] (double-buffered by tile parity)
+    int32_t* s_trow = reinterpret_cast<int32_t*>(smem + cfg::kTokOff);
+    float* s_tlg = reinterpret_cast<float*>(smem + cfg::kTokOff + 2 * 128 * 4);
     int acc_i = 0;
     Seg sg;
     bool bad_row = false;
@@ -749,6 +753,18 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       int t0, T;
       groups.info(sg.g, e, t0, T);
       const int buf = acc_i & 1;
+      // the tile's out rows and logits, one token per epilogue thread, fetched before the
+      // accumulator is ready (fetched per 32-token chunk after it, each chunk waited an L2 round
+      // trip: 128-token tiles ended their CTA's work several microseconds late).  Every epilogue
+      // warp reaches this barrier on every tile (they walk the same items), and a warp that is
+      // one tile ahead writes the other buffer.
+      if (ep_tid < T) {
+        const int row = load_row32(p.row_index, p.row_i32, (int64_t)t0 + ep_tid, p.batch);
+        s_trow[buf * 128 + ep_tid] = row;
+        s_tlg[buf * 128 + ep_tid] = p.logit ? p.logit[t0 + ep_tid] : 1.f;
+        bad_row |= row < 0;
+      }
+      ptx::bar_sync(1, 128);
       const uint32_t aph = (acc_i >> 1) & 1;
       if (!warp_wait_bar(ptx::smem_u32(&accf[buf]), aph, ctl)) break;
       ptx::tc_fence_after();
@@ -758,14 +774,6 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       const float bias_n = (p.bias != nullptr && sg.kb0 == 0 && n_ok) ? bf16f(p.bias[(int64_t)e * p.N + n]) : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * tmax;
       for (int c0 = 0; c0 < T; c0 += 32) {
-        const int tok = c0 + lane;
-        int my_row = -1;
-        float my_lg = 0.f;
-        if (tok < T) {
-          my_row = load_row32(p.row_index, p.row_i32, (int64_t)t0 + tok, p.batch);
-          my_lg = p.logit ? p.logit[t0 + tok] : 1.f;
-          bad_row |= my_row < 0;
-        }
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(taddr + c0, v);
         ptx::tmem_wait_ld();
@@ -775,25 +783,22 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
           if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acce[buf]));
         }
         const int cnt = T - c0 < 32 ? T - c0 : 32;
+        const int32_t* rows = s_trow + buf * 128 + c0;  // read as broadcasts
+        const float* lgs = s_tlg + buf * 128 + c0;
         // one unrolled loop per mode, so the atomic mode's hot code holds no store path of
         // the deterministic one (the instruction cache is the scarce resource here)
         if constexpr (det) {
           float* y = p.ybuf + ((int64_t)sg.slot * p.M + t0 + c0) * p.N + n;
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            if (jj < cnt) {
-              const float lg = __shfl_sync(0xffffffffu, my_lg, jj);
-              if (n_ok) y[(int64_t)jj * p.N] = (__uint_as_float(v[jj]) + bias_n) * lg;
-            }
-          }
+          for (int jj = 0; jj < 32; ++jj)
+            if (jj < cnt && n_ok) y[(int64_t)jj * p.N] = (__uint_as_float(v[jj]) + bias_n) * lgs[jj];
         } else {
           float* o = p.out + n;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             if (jj < cnt) {
-              const int row = __shfl_sync(0xffffffffu, my_row, jj);
-              const float lg = __shfl_sync(0xffffffffu, my_lg, jj);
-              if (n_ok && row >= 0) ptx::red_add_f32(o + (int64_t)row * p.N, (__uint_as_float(v[jj]) + bias_n) * lg);
+              const int row = rows[jj];
+              if (n_ok && row >= 0) ptx::red_add_f32(o + (int64_t)row * p.N, (__uint_as_float(v[jj]) + bias_n) * lgs[jj]);
             }
           }
         }
