@@ -15,6 +15,7 @@ Prints one JSON line on rank 0.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -154,13 +155,14 @@ def _oracle_problem(spec, inp, ncols):
         x2s = x2[:, :, :(ncols // 2 if spec.x2_dtype == W.E2M1 else ncols)].contiguous()
         scs = sc[..., :ncols, :].contiguous()
     shared = inp["shared_input"][:, :ncols].contiguous() if inp["shared_input"] is not None else None
+    bias = inp["bias"][:, :ncols].contiguous() if inp.get("bias") is not None else None
     return oracle.Problem(M=spec.M, K=spec.K, N=ncols, E=spec.E, batch=spec.batch, x1=inp["x1"].cpu(), x2=x2s,
                           scale=scs, pertoken_scale=inp["pertoken_scale"].cpu(), group_list=inp["group_list"].cpu(),
                           row_index=inp["row_index"].cpu(), out=inp["out"].cpu()[:, :ncols].contiguous(),
                           x1_dtype=spec.x1_dtype, x2_dtype=spec.x2_dtype, transpose_x2=spec.transpose_x2,
                           scale_per_expert=spec.scale_per_expert, group_list_type=spec.group_list_type,
                           logit=inp["logit"].cpu() if inp["logit"] is not None else None, shared_input=shared,
-                          shared_offset=spec.shared_offset, shared_weight=spec.shared_weight)
+                          shared_offset=spec.shared_offset, shared_weight=spec.shared_weight, bias=bias)
 
 
 def _cpu_baseline(spec, inp, min_s=10.0, max_s=30.0):
@@ -418,14 +420,18 @@ def run_reference(args):
 
 def _main_spec(args):
     """The workload of the timed call: --config N, or with --fp4 the MXFP4 operator at the
-    large shape (c5) or its reduced copy (e32)."""
+    large shape (c5) or its reduced copy (e32); --bias adds the per-expert bf16 bias."""
     from moe_grouped_gemm_mxfp8_gb300 import workloads as W
 
     if args.fp4 == "c5":
-        return W.mxfp4_config()
-    if args.fp4 == "e32":
-        return W.mxfp4_small_config()
-    return W.config(args.config)
+        spec = W.mxfp4_config()
+    elif args.fp4 == "e32":
+        spec = W.mxfp4_small_config()
+    else:
+        spec = W.config(args.config)
+    if args.bias:
+        spec = dataclasses.replace(spec, name=spec.name + " bias", bias=True)
+    return spec
 
 
 def run_ours(args):
@@ -452,6 +458,7 @@ def run_ours(args):
     inp = W.make_inputs(spec, device="cpu", weights_device="cuda")
     d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
     prob = B.problem_from_spec(spec, args.deterministic)
+    prob.expected_tokens_per_expert = args.tokens_hint  # the tuning hint (0: chosen on the device)
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
 
@@ -647,6 +654,9 @@ def main():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--fp4", default="off", choices=["off", "c5", "e32"],
                     help="time the MXFP4 (E2M1) operator instead: the large shape, or its 32-expert copy")
+    ap.add_argument("--bias", action="store_true", help="add the per-expert bf16 bias input")
+    ap.add_argument("--tokens-hint", type=int, default=0,
+                    help="expected_tokens_per_expert tuning hint (fixes the token group width)")
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

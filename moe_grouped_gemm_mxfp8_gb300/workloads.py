@@ -249,7 +249,8 @@ def mxfp4_small_config() -> Spec:
 def algorithmic_bytes(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:
     """Bytes a single call must move at minimum: x2 (and its scales) of every
     expert that holds a token, x1, pertoken_scale, logit, row_index,
-    group_list, shared_input, and out read once and written once."""
+    group_list, shared_input, the bias rows of those experts, and out read once
+    and written once."""
     if counts is None:
         counts = expert_counts(spec)
     nnz = int((counts > 0).sum())
@@ -260,7 +261,8 @@ def algorithmic_bytes(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:
     tok = covered * (K // 2 if spec.x1_dtype == E2M1 else K) + covered * Ks * 2 + covered * 4 * (0 if spec.logit == "none" else 1) + covered * 8
     shared = spec.n_shared * N * 2
     out = spec.batch * N * 4 * 2
-    return w + tok + shared + out + spec.E * 8
+    bias = nnz * N * 2 if spec.bias else 0
+    return w + tok + shared + out + spec.E * 8 + bias
 
 
 def flops(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:

@@ -26,6 +26,7 @@ BASE = W.Spec("sample", batch=12, M=24, K=96, N=40, E=3, rows="random", shared_r
     dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1),
     dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, transpose_x2=True),
     dict(x2_dtype=W.E2M1, scale_per_expert=True),
+    dict(bias=True, transpose_x2=True),
 ])
 def test_column_sample_equals_full_run(kw):
     spec = dataclasses.replace(BASE, **kw)
