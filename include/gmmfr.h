@@ -174,6 +174,10 @@ GMMFR_API gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int ha
  * The grouped GEMM is launched as a programmatic dependent of the previous kernel in
  * `stream`: when that kernel allows it (gmmfr_moe_route does), the GEMM's launch
  * overlaps its tail; the GEMM reads no input before that kernel has completed.
+ * Kernels per call: the grouped GEMM alone in the default mode; with
+ * GMMFR_DETERMINISTIC the GEMM (which also builds the row CSR of the tokens) and then
+ * the combine, a programmatic dependent of the GEMM.  Weights prepared inside the call
+ * add the preparation kernel first, and an expanded E2M1 x1 the expansion kernel.
  */
 GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing(
     const gmmfr_problem* problem, const void* x1, const void* x2, const void* scale,
@@ -252,8 +256,8 @@ GMMFR_API gmmfr_status gmmfr_moe_route_workspace_size(const gmmfr_route_problem*
  *            x [batch, K] FP8 bytes; x_scale [batch, ceil(K/64), 2] E8M0 bytes
  *   outputs  x1 [M, K]; pertoken_scale [M, ceil(K/64), 2]; group_list [E] int64;
  *            row_index [M] int64; logit [M] float32 or NULL; perm [M] int32 or NULL
- * Three kernel launches; never syncs, never allocates.  Bit-exact and
- * deterministic (byte and index work only).
+ * One kernel launch up to 8192 entries (M), three above; never syncs, never allocates.
+ * Bit-exact and deterministic (byte and index work only).
  */
 GMMFR_API gmmfr_status gmmfr_moe_route(const gmmfr_route_problem* problem, const void* topk_ids,
                                        const float* topk_weights, const void* x, const void* x_scale, void* x1,
