@@ -226,17 +226,62 @@ constexpr int kCombineCap = 2048;  // row segments up to this length are ordered
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
+// Four consecutive floats from column n0 on (one 16-byte load when `vec`, i.e. N % 4 == 0 and
+// 16-byte aligned rows); columns past N read 0.
+template <bool vec>
+__device__ __forceinline__ float4 ld4(const float* row, int64_t n0, int64_t N) {
+  if constexpr (vec) return n0 < N ? *reinterpret_cast<const float4*>(row + n0) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 v;
+  v.x = n0 < N ? row[n0] : 0.f;
+  v.y = n0 + 1 < N ? row[n0 + 1] : 0.f;
+  v.z = n0 + 2 < N ? row[n0 + 2] : 0.f;
+  v.w = n0 + 3 < N ? row[n0 + 3] : 0.f;
+  return v;
+}
+
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+
+// c_t for four columns: Y[0][t] + Y[1][t] + ... over the K splits
+template <bool vec>
+__device__ __forceinline__ float4 token_sum(const CombineParams& p, int t, int64_t n0) {
+  float4 v = ld4<vec>(p.ybuf + (int64_t)t * p.N, n0, p.N);
+  for (int s = 1; s < p.split; ++s) add4(v, ld4<vec>(p.ybuf + ((int64_t)s * p.M + t) * p.N, n0, p.N));
+  return v;
+}
+
 // out[r, n] = ((out[r, n] + c_t1) + c_t2) + ... + w * shared[r - offset, n], the tokens
 // t1 < t2 < ... of row r in ascending order, c_t = Y[0][t][n] + Y[1][t][n] + ...
+// vec: N % 4 == 0 with 16-byte aligned out and Y rows and 8-byte aligned shared_input rows
+template <bool vec>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
   __shared__ int32_t s_tok[kCombineCap];
   __shared__ int32_t s_ord[kCombineCap];
   __shared__ int32_t s_min[kCombineThreads / 32];
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int64_t n0 = ((int64_t)blockIdx.y * kCombineThreads + tid) * 4;
+  // out and shared_input are not written by the grouped GEMM in this mode (it writes Y and
+  // the row CSR only), so this block reads them while that kernel may still be running
+  float4 acc = ld4<vec>(p.out + r * p.N, n0, p.N);
+  const bool has_shared = p.shared && r >= p.shared_offset && r < p.shared_offset + p.shared_rows;
+  uint2 sh = make_uint2(0, 0);  // four bf16 values, low half first
+  if (has_shared) {
+    const uint16_t* srow = p.shared + (r - p.shared_offset) * p.N;
+    if constexpr (vec) {
+      if (n0 < p.N) sh = *reinterpret_cast<const uint2*>(srow + n0);
+    } else {
+      sh.x = (n0 < p.N ? srow[n0] : 0u) | (n0 + 1 < p.N ? (uint32_t)srow[n0 + 1] << 16 : 0u);
+      sh.y = (n0 + 2 < p.N ? srow[n0 + 2] : 0u) | (n0 + 3 < p.N ? (uint32_t)srow[n0 + 3] << 16 : 0u);
+    }
+  }
   // launched as a programmatic dependent of the grouped GEMM: Y and the row CSR are read only
   // after that kernel has completed
   ptx::griddep_wait();
-  const int64_t r = blockIdx.x;
-  const int tid = threadIdx.x;
   const int beg = p.row_ptr[r];
   const int L = p.row_ptr[r + 1] - beg;
   const bool in_smem = L <= kCombineCap;
@@ -250,17 +295,18 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
       s_ord[rank] = t;
     }
     __syncthreads();
-  }
-  const int64_t n0 = ((int64_t)blockIdx.y * kCombineThreads + tid) * 4;
-  float acc[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) acc[c] = (n0 + c < p.N) ? p.out[r * p.N + n0 + c] : 0.f;
-  int prev = -1;
-  for (int i = 0; i < L; ++i) {
-    int t;
-    if (in_smem) {
-      t = s_ord[i];
-    } else {  // long segment: select the next larger token with a block-wide minimum
+    // two tokens' loads in flight at a time; the sums stay in ascending token order
+    int i = 0;
+    for (; i + 1 < L; i += 2) {
+      const float4 a = token_sum<vec>(p, s_ord[i], n0);
+      const float4 b = token_sum<vec>(p, s_ord[i + 1], n0);
+      add4(acc, a);
+      add4(acc, b);
+    }
+    if (i < L) add4(acc, token_sum<vec>(p, s_ord[i], n0));
+  } else {
+    int prev = -1;
+    for (int i = 0; i < L; ++i) {  // long segment: select the next larger token with a block-wide minimum
       int m = 0x7fffffff;
       for (int j = tid; j < L; j += kCombineThreads) {
         const int u = p.sorted[beg + j];
@@ -273,26 +319,25 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
       m = s_min[0];
       for (int w = 1; w < kCombineThreads / 32; ++w) m = min(m, s_min[w]);
       __syncthreads();
-      t = m;
       prev = m;
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (n0 + c < p.N) {
-        float v = p.ybuf[(int64_t)t * p.N + n0 + c];
-        for (int s = 1; s < p.split; ++s) v += p.ybuf[((int64_t)s * p.M + t) * p.N + n0 + c];
-        acc[c] += v;
-      }
+      add4(acc, token_sum<vec>(p, m, n0));
     }
   }
-  if (p.shared && r >= p.shared_offset && r < p.shared_offset + p.shared_rows) {
+  if (has_shared) {
+    acc.x += p.shared_weight * bf16_to_f32(sh.x & 0xFFFF);
+    acc.y += p.shared_weight * bf16_to_f32(sh.x >> 16);
+    acc.z += p.shared_weight * bf16_to_f32(sh.y & 0xFFFF);
+    acc.w += p.shared_weight * bf16_to_f32(sh.y >> 16);
+  }
+  float* orow = p.out + r * p.N;
+  if constexpr (vec) {
+    if (n0 < p.N) *reinterpret_cast<float4*>(orow + n0) = acc;
+  } else {
+    const float a[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      if (n0 + c < p.N) acc[c] += p.shared_weight * bf16_to_f32(p.shared[(r - p.shared_offset) * p.N + n0 + c]);
+      if (n0 + c < p.N) orow[n0 + c] = a[c];
   }
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    if (n0 + c < p.N) p.out[r * p.N + n0 + c] = acc[c];
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
@@ -309,7 +354,11 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, combine_kernel, p);
+  // 16-byte loads and stores of out and Y rows, 8-byte loads of shared_input rows
+  const bool vec = p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15) == 0 &&
+                  (reinterpret_cast<uintptr_t>(p.ybuf) & 15) == 0 &&
+                  (reinterpret_cast<uintptr_t>(p.shared) & 7) == 0;
+  return vec ? cudaLaunchKernelEx(&lc, combine_kernel<true>, p) : cudaLaunchKernelEx(&lc, combine_kernel<false>, p);
 }
 
 }  // namespace gmmfr

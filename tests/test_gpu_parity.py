@@ -182,8 +182,11 @@ def test_small_atomic(name):
     check_full(_spec(**SMALL[name]), W.make_inputs(_spec(**SMALL[name])))
 
 
+# k16_n1, mxfp4_k96 (N 130) and e4m3_tokens_mxfp4_weights (N 255): N % 4 != 0, the combine's
+# scalar path
 @pytest.mark.parametrize("name", ["basic", "transposed", "ragged_counts", "random_rows_shared", "straddle", "k96",
-                                  "bias_split_k", "mxfp4_t", "mxfp4_k352_bias"])
+                                  "bias_split_k", "mxfp4_t", "mxfp4_k352_bias", "k16_n1", "mxfp4_k96",
+                                  "e4m3_tokens_mxfp4_weights"])
 def test_small_deterministic(name):
     spec = _spec(**SMALL[name])
     inp = W.make_inputs(spec)
@@ -421,6 +424,37 @@ def test_deterministic_many_tokens():
     spec = W.Spec("det many tokens", batch=3000, M=9000, K=128, N=256, E=8, rows="random", counts="multinomial",
                   shared_rows=100, shared_offset=7, shared_weight=0.3, out_init="randn", seed=77)
     check_full(spec, W.make_inputs(spec), deterministic=True)
+
+
+def test_deterministic_rows_of_more_than_2048_tokens():
+    """Two output rows holding about 2200 routed tokens each: the combine orders a row's tokens by
+    a block-wide minimum per token instead of in shared memory (rows of up to 2048 tokens)."""
+    spec = W.Spec("det long rows", batch=2, M=4400, K=64, N=192, E=3, rows="random", counts="multinomial",
+                  shared_rows=1, shared_offset=1, shared_weight=0.5, out_init="randn", seed=78)
+    inp = W.make_inputs(spec)
+    assert np.bincount(inp["row_index"].numpy(), minlength=2).min() > 2048
+    got, _ = check_full(spec, inp, deterministic=True)
+    again, _ = gpu_run(spec, inp, deterministic=True)
+    assert np.array_equal(got, again)
+
+
+def test_deterministic_unaligned_out_and_shared():
+    """out 4 bytes and shared_input 2 bytes past an aligned base (N % 4 == 0): the combine's scalar
+    path, with the same results as the vector path bit for bit."""
+    spec = _spec(rows="random", shared_rows=6, shared_offset=5, shared_weight=0.7, out_init="randn")
+    inp = W.make_inputs(spec)
+    d = _dev(inp)
+    aligned, _ = check_full(spec, inp, deterministic=True)
+    prob = B.problem_from_spec(spec, True)
+    prep = B.prepare_weights(prob, d["x2"], d["scale"])
+    n_out, n_sh = d["out"].numel(), d["shared_input"].numel()
+    out = torch.empty(n_out + 4, device="cuda")[1:1 + n_out].view(d["out"].shape)
+    out.copy_(d["out"])
+    shared = torch.empty(n_sh + 8, dtype=torch.bfloat16, device="cuda")[1:1 + n_sh].view(d["shared_input"].shape)
+    shared.copy_(d["shared_input"])
+    ws = B.run(prob, dict(d, shared_input=shared), out, prepared=prep)
+    assert B.gmmfr_check_device_errors(ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    assert np.array_equal(out.cpu().numpy().astype(np.float64), aligned)
 
 
 def test_config4_deterministic_bit_stable():
