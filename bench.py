@@ -194,9 +194,12 @@ def _cpu_baseline(spec, inp, min_s=10.0, max_s=30.0):
     return gbs, dt, f"oracle on {what}, {reps} run(s), {dt:.1f} s", threads
 
 
-def _profiled_traffic(workload):
+def _profiled_traffic(workload, as_captured=True):
     """DRAM bytes per gemm_kernel launch from the committed ncu summary of this
-    workload, if the kernel sources are unchanged since that capture (else None)."""
+    workload, if the kernel sources are unchanged since that capture and the run is set up
+    as it was (atomic mode, no bias, no tiling hint: `as_captured`); else None."""
+    if not as_captured:
+        return None
     import hashlib
     path = os.path.join(ROOT, "profiles", "gemm_kernel_" + workload.split()[0] + ".md")
     try:
@@ -618,7 +621,8 @@ def run_ours(args):
         "weight_prep_ms": prep_ms,
         "weight_prep_gbs": 2 * n_prep / (prep_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": gemm_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": gemm_gbs / hbm_peak, "traffic": _profiled_traffic(spec.name),
+                     "frac": gemm_gbs / hbm_peak, "traffic": _profiled_traffic(
+                         spec.name, not (args.deterministic or spec.bias or args.tokens_hint)),
                      "kernel": "gemm_kernel (grouped GEMM + fused epilogue)",
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
         "e2e": {"value": alg_bytes / (e2e_serial_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
