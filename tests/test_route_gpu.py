@@ -51,6 +51,26 @@ def test_route_bit_exact(kw, ids32, glt):
         assert np.array_equal(got.reshape(ref[k].shape).astype(ref[k].dtype), ref[k]), k
 
 
+@pytest.mark.parametrize("run", [80, 1000])
+def test_route_runs_of_equal_ids(run):
+    """Expert ids in runs of equal values (80: runs that start and end inside warps of 32
+    entries; 1000: most warps hold one id), with invalid ids in one run: warps whose 32 keys
+    are equal are counted in one step, the others entry by entry."""
+    batch, topk, E = 1500, 2, 6
+    spec = W.RouteSpec("t", batch=batch, topk=topk, K=96, E=E, seed=run)
+    inp = W.make_route_inputs(spec)
+    flat = (np.arange(batch * topk) // run) % E
+    flat[2 * run:3 * run] = E + 2  # the third run: invalid ids
+    ids = torch.from_numpy(flat.reshape(batch, topk).astype(np.int64))
+    ref = R.moe_route(ids.numpy(), inp["topk_weights"].numpy(), inp["x"].numpy(), inp["x_scale"].numpy(), E, 1)
+    out, ws = B.route(ids.cuda(), inp["topk_weights"].cuda(), inp["x"].cuda(), inp["x_scale"].cuda(), E, 1)
+    bits = B.gmmfr_check_device_errors(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert bits == B.DEV_BAD_EXPERT_ID and ref["flags"]
+    for k in ("perm", "x1", "pertoken_scale", "group_list", "row_index", "logit"):
+        got = out[k].cpu().numpy()
+        assert np.array_equal(got.reshape(ref[k].shape).astype(ref[k].dtype), ref[k]), k
+
+
 @pytest.mark.parametrize("kw", [CASES[1], CASES[2], CASES[4], CASES[5]], ids=["1", "2", "4", "5"])
 def test_route_three_launch_path_bit_exact(kw, monkeypatch):
     """Below 8193 entries the library routes in one launch; the three-launch path
