@@ -231,6 +231,8 @@ def test_int32_row_index_and_raw_weights():
 def test_m_zero_adds_only_shared():
     spec = _spec(M=0, E=3, counts="explicit", explicit_counts=(0, 0, 0), out_init="randn")
     check_full(spec, W.make_inputs(spec))
+    # deterministic mode: an empty row CSR, the combine adds the shared rows alone
+    check_full(spec, W.make_inputs(spec), deterministic=True)
 
 
 def test_nan_scale_code_propagates():
