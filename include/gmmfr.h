@@ -77,7 +77,7 @@ typedef enum { GMMFR_INDEX_I64 = 0, GMMFR_INDEX_I32 = 1 } gmmfr_index_type;
  * section 5.1 FinalizeRoutingConfig fields).
  *
  *   M      rows of x1, pertoken_scale, logit, row_index (routed tokens, batch*topk); M >= 0
- *   K      contraction length, K >= 1 (this build needs K % 16 == 0)
+ *   K      contraction length, K >= 1 and K % 16 == 0
  *   N      output columns, N >= 0
  *   E      experts, 1 <= E <= 1024 (aclnn V3 constraint "e <= 1024")
  *   batch  rows of out, batch >= 0

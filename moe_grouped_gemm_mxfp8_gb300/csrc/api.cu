@@ -61,7 +61,7 @@ gmmfr_status validate(const gmmfr_problem* p) {
     return fail(GMMFR_ERR_INVALID_ARG, "expected_tokens_per_expert=%lld is negative", (long long)p->expected_tokens_per_expert);
   if (p->x2_format == GMMFR_E2M1 && !p->transpose_x2 && p->N % 2 != 0)
     return fail(GMMFR_ERR_INVALID_ARG, "N=%lld: an E2M1 x2 that is not transposed needs an even N", (long long)p->N);
-  if (p->K % 16 != 0) return fail(GMMFR_ERR_UNSUPPORTED, "K=%lld: this build needs K %% 16 == 0 (x1 rows are moved by TMA)", (long long)p->K);
+  if (p->K % 16 != 0) return fail(GMMFR_ERR_UNSUPPORTED, "K=%lld: K %% 16 == 0 is required (x1 rows are moved by TMA)", (long long)p->K);
   return GMMFR_OK;
 }
 
