@@ -60,7 +60,9 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # GMMFR_ORACLE_LIB: another build of gmmfr_oracle.c (the mutation test plants
+            # mistakes in copies of it and checks that the pins catch each)
+            lib = ctypes.CDLL(os.environ.get("GMMFR_ORACLE_LIB") or build())
             P = ctypes.POINTER(_Args)
             lib.oracle_decode_fp8.restype = ctypes.c_double
             lib.oracle_decode_fp8.argtypes = [ctypes.c_int, ctypes.c_uint32]
