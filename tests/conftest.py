@@ -1,3 +1,4 @@
+import importlib
 import os
 import sys
 
@@ -8,3 +9,14 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    # the oracle mutation test: GMMFR_ORACLE_PY_MUTANT = "<module>=<path>" runs the pins with the
+    # functions of <module> (an oracle module) replaced by those of a mutated copy of its source
+    spec = os.environ.get("GMMFR_ORACLE_PY_MUTANT")
+    if spec:
+        name, path = spec.split("=", 1)
+        mod = importlib.import_module(name)
+        ns = {"__name__": name + "_mutant"}
+        exec(compile(open(path).read(), path, "exec"), ns)
+        for k, v in ns.items():
+            if callable(v) and getattr(v, "__module__", None) == ns["__name__"]:
+                setattr(mod, k, v)

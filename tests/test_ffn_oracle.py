@@ -55,6 +55,34 @@ def test_closed_form_one_hot():
     assert np.all(r["result"][:, I:] == 0)
 
 
+def test_both_bf16_casts_match_torch():
+    """sw = bf16(SiLU(gate) * up) and result = bf16(sw @ w2_e), each cast checked against torch's
+    own float64 -> bfloat16 conversion (the intermediate and the output are BF16, LLaDA2.0-mini
+    grouped-GEMM write-up, section 3.3).  Small-integer tokens and weights (over 16) keep every
+    sum exact in float64, so both sides round the same values."""
+    H, I, n = 64, 48, (7, 9)
+    E = len(n)
+    rng = np.random.default_rng(5)
+    x = rng.integers(-3, 4, (sum(n), H)).astype(np.float64)
+    w13 = rng.integers(-4, 5, (E * H, 2 * I)).astype(np.float64) / 16
+    w2 = rng.integers(-4, 5, (E * I, H)).astype(np.float64) / 16
+    cs = np.concatenate([[0], np.cumsum(n)])
+    r = F.grouped_swiglu_ffn(F.f64_to_bf16_bits(x), F.f64_to_bf16_bits(w13), F.f64_to_bf16_bits(w2), cs, H, I)
+    t64 = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    bf = lambda t: t.to(torch.bfloat16).to(torch.float64).numpy()
+    cast_moved = [False, False]  # each cast changes some value here, so a missing one shows
+    for e in range(E):
+        s, t = cs[e], cs[e + 1]
+        gate, up = (t64(x[s:t]) @ t64(w13[e * H:(e + 1) * H])).split(I, dim=1)
+        sw = torch.nn.functional.silu(gate) * up
+        assert np.array_equal(r["sw"][s:t], bf(sw))
+        down = t64(r["sw"][s:t]) @ t64(w2[e * I:(e + 1) * I])
+        assert np.array_equal(r["result"][s:t], bf(down))
+        cast_moved[0] |= not np.array_equal(bf(sw), sw.numpy())
+        cast_moved[1] |= not np.array_equal(bf(down), down.numpy())
+    assert all(cast_moved)
+
+
 @pytest.mark.parametrize("counts", [(0, 1, 2, 4, 8, 16, 32, 0), (5, 0, 3), (1,)])
 def test_against_torch_float64_restatement(counts):
     spec = W.FfnSpec("t", H=128, I=64, E=len(counts), counts=counts, scale=0.3, seed=len(counts))

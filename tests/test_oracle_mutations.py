@@ -1,8 +1,12 @@
-"""The pins have teeth: a plausible mistake planted in a copy of the oracle's C source
-(a wrong scale index or layout stride, a wrong exponent bias, a dropped or misplaced term, a
-wrong sign, an off-by-one range, swapped nibbles) makes at least one pin of
-test_oracle_pins.py fail.  Each mutant is built with the oracle's own compiler flags and
-run through the pins in a child process (GMMFR_ORACLE_LIB points the oracle at it)."""
+"""The pins have teeth: a plausible mistake planted in a copy of an oracle's source makes at
+least one of its pins fail.
+  - The operator's C oracle (a wrong scale index or layout stride, a wrong exponent bias, a
+    dropped or misplaced term, a wrong sign, an off-by-one range, swapped nibbles): each mutant
+    is built with the oracle's own compiler flags and run through test_oracle_pins.py in a
+    child process (GMMFR_ORACLE_LIB points the oracle at it).
+  - The routing and FFN oracles (numpy): the pins of test_route_oracle.py / test_ffn_oracle.py
+    run in a child process whose conftest swaps in the functions of the mutated source
+    (GMMFR_ORACLE_PY_MUTANT)."""
 import concurrent.futures as cf
 import os
 import shutil
@@ -65,6 +69,66 @@ def test_every_planted_mistake_fails_a_pin(tmp_path):
         caught = list(ex.map(_pins_fail, libs))
     survivors = [m[0] for m, c in zip(MUTANTS, caught) if not c]
     assert not survivors, f"mutants no pin catches: {survivors}"
+
+
+# (module, pins, name, text in the module's source (exactly once), replacement)
+PY_MUTANTS = [
+    ("oracle.route", "test_route_oracle.py", "invalid ids sorted first", "key = np.where(valid, flat, E)",
+     "key = np.where(valid, flat, -1)"),
+    ("oracle.route", "test_route_oracle.py", "ties in descending entry order",
+     'perm = np.argsort(key, kind="stable").astype(np.int64)',
+     'perm = (key.size - 1 - np.argsort(key[::-1], kind="stable")).astype(np.int64)'),
+    ("oracle.route", "test_route_oracle.py", "group_list types swapped",
+     "group_list = counts if group_list_type == 1 else np.cumsum(counts)",
+     "group_list = np.cumsum(counts) if group_list_type == 1 else counts"),
+    ("oracle.route", "test_route_oracle.py", "invalid ids counted", "np.bincount(flat[valid], minlength=E)",
+     "np.bincount(np.clip(flat, 0, E - 1), minlength=E)"),
+    ("oracle.route", "test_route_oracle.py", "rows not permuted", "src_row = perm // topk",
+     "src_row = np.arange(perm.size) // topk"),
+    ("oracle.route", "test_route_oracle.py", "logit not permuted", "else w[perm],", "else w,"),
+    ("oracle.ffn", "test_ffn_oracle.py", "SiLU sign", "g / (1.0 + np.exp(-g))", "g / (1.0 + np.exp(g))"),
+    ("oracle.ffn", "test_ffn_oracle.py", "gate and up swapped", "silu(gu[:, :I]) * gu[:, I:]",
+     "silu(gu[:, I:]) * gu[:, :I]"),
+    ("oracle.ffn", "test_ffn_oracle.py", "sw not cast to bf16", "sw = round_bf16(silu(gu[:, :I]) * gu[:, I:])",
+     "sw = silu(gu[:, :I]) * gu[:, I:]"),
+    ("oracle.ffn", "test_ffn_oracle.py", "result not cast to bf16", "res[s:t] = round_bf16(sw @ w2e)",
+     "res[s:t] = sw @ w2e"),
+    ("oracle.ffn", "test_ffn_oracle.py", "bf16 with 7 significant bits", "r = np.round(m * 256.0)",
+     "r = np.round(m * 128.0) * 2"),
+    ("oracle.ffn", "test_ffn_oracle.py", "ties away from zero", "r = np.round(m * 256.0)",
+     "r = np.trunc(m * 256.0 + np.sign(m) * 0.5)"),
+    ("oracle.ffn", "test_ffn_oracle.py", "w2 of expert 0 for every expert", "w2e = w2[e * I:(e + 1) * I]",
+     "w2e = w2[0:I]"),
+    ("oracle.ffn", "test_ffn_oracle.py", "expert range one row short", "s, t = int(cs[e]), int(cs[e + 1])",
+     "s, t = int(cs[e]), int(cs[e + 1]) - (1 if cs[e + 1] > cs[e] else 0)"),
+]
+
+
+def _py_pins_fail(tmp, i, module, pins, old, new):
+    src_path = os.path.join(ROOT, *module.split(".")) + ".py"
+    src = open(src_path).read()
+    assert src.count(old) == 1, old
+    path = os.path.join(tmp, f"py{i}.py")
+    open(path, "w").write(src.replace(old, new))
+    env = dict(os.environ, GMMFR_ORACLE_PY_MUTANT=f"{module}={path}", OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", pins), "-x", "-q",
+                        "-p", "no:cacheprovider"], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    return r.returncode == 1 and " failed" in r.stdout
+
+
+def test_every_planted_mistake_in_the_numpy_oracles_fails_a_pin(tmp_path):
+    with cf.ThreadPoolExecutor(min(8, os.cpu_count() or 1)) as ex:
+        caught = list(ex.map(lambda a: _py_pins_fail(str(tmp_path), *a),
+                             [(i, m[0], m[1], m[3], m[4]) for i, m in enumerate(PY_MUTANTS)]))
+    survivors = [m[2] for m, c in zip(PY_MUTANTS, caught) if not c]
+    assert not survivors, f"mutants no pin catches: {survivors}"
+    # the unmodified sources pass their pins by the same route
+    for module, pins in (("oracle.route", "test_route_oracle.py"), ("oracle.ffn", "test_ffn_oracle.py")):
+        path = os.path.join(ROOT, *module.split(".")) + ".py"
+        env = dict(os.environ, GMMFR_ORACLE_PY_MUTANT=f"{module}={path}", OMP_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", pins), "-q",
+                            "-p", "no:cacheprovider"], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stdout[-2000:]
 
 
 def test_the_unmodified_source_passes_through_the_same_route(tmp_path):
