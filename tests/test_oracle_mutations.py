@@ -36,6 +36,20 @@ MUTANTS = [
     ("count ranges restart at 0", "const int64_t s = prev_end;", "const int64_t s = 0;"),
     ("prefix-sum end off by one", "t = g < s ? s : (g > a->M ? a->M : g);",
      "t = g < s ? s : (g > a->M ? a->M : (g > s ? g - 1 : g));"),
+    ("E2M1 subnormal step", "e == 0 ? 0.5 * m :", "e == 0 ? 1.0 * m :"),
+    ("E2M1 exponent bias", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e - 2)"),
+    ("E5M2 infinity read as NaN", "return s ? -INFINITY : INFINITY;", "return NAN;"),
+    ("E8M0 NaN code read as a power of two", "if (code == 255) return NAN;", "if (code == 256) return NAN;"),
+    ("per-expert scale stride", "e * Ks * a->N * 2 : 0;", "e * Ks * a->N : 0;"),
+    ("transposed x2 read untransposed", "if (a->transpose_x2) return element_code(", "if (0) return element_code("),
+    ("bias of expert 0 for every expert", "a->bias[e * N + n0 + j]", "a->bias[n0 + j]"),
+    ("shared rows placed from row 0", "const int64_t r = a->shared_offset + i;", "const int64_t r = i;"),
+    ("bad row index not flagged", "flags |= ORACLE_BAD_ROW_INDEX;", "flags |= 0;"),
+    ("count past M not flagged", "if (g < 0 || g > a->M - s) flags |= ORACLE_BAD_GROUP_LIST;",
+     "if (g < 0) flags |= ORACLE_BAD_GROUP_LIST;"),
+    ("sampled path drops the logit", "v += lg * (acc + b);", "v += acc + b;"),
+    ("sampled path drops the shared weight", "v += a->shared_weight * oracle_decode_bf16(",
+     "v += oracle_decode_bf16("),
 ]
 
 

@@ -328,6 +328,11 @@ def test_expert_ranges_closed_form():
 @pytest.mark.parametrize("gtype,gl,exp_start,exp_end", [
     (1, [3, -2, 4, 9], [0, 3, 3, 7], [3, 3, 7, 10]),   # negative count, total > M
     (0, [3, 2, 7, 12], [0, 3, 3, 7], [3, 3, 7, 10]),   # decreasing prefix, last > M
+    # one fault at a time: each alone raises the flag
+    (1, [3, 0, 4, 9], [0, 3, 3, 7], [3, 3, 7, 10]),    # total > M
+    (1, [3, -2, 4, 3], [0, 3, 3, 7], [3, 3, 7, 10]),   # negative count
+    (0, [3, 2, 7, 10], [0, 3, 3, 7], [3, 3, 7, 10]),   # decreasing prefix
+    (0, [3, 3, 7, 12], [0, 3, 3, 7], [3, 3, 7, 10]),   # last prefix > M
 ])
 def test_invalid_group_list_is_flagged_and_clamped(gtype, gl, exp_start, exp_end):
     spec = _spec(E=4, M=10, group_list_type=gtype)
@@ -439,7 +444,7 @@ def test_bias_closed_form():
 
 
 def test_sampled_equals_full():
-    spec = _spec(rows="random", out_init="randn", shared_rows=3, shared_offset=1, bias=True)
+    spec = _spec(rows="random", out_init="randn", shared_rows=3, shared_offset=1, shared_weight=0.7, bias=True)
     inp = W.make_inputs(spec)
     p = oracle.problem_from_spec(spec, inp)
     out, absb, _ = oracle.run(p)
