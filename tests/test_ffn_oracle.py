@@ -53,6 +53,25 @@ def test_closed_form_one_hot():
     exp = F.round_bf16(ga / (1 + np.exp(-ga)) * gb)
     assert np.array_equal(r["result"][:, :I], np.tile(exp, (3, 1)))
     assert np.all(r["result"][:, I:] == 0)
+    # absb = |sw| @ |w2|: here |sw| on the first I columns, 0 beyond
+    assert np.array_equal(r["absb"][:, :I], np.tile(np.abs(exp), (3, 1)))
+    assert np.all(r["absb"][:, I:] == 0)
+
+
+def test_tolerance_admits_one_bf16_step():
+    """With no sw term, the bound on a bf16 result r (|r| >= 1, where the 1e-7 floor is
+    negligible) is at least the gap to the next bf16 value above |r| and less than twice it
+    (two values a rounding apart land on adjacent bf16 values; a looser bound would hide a
+    wrong rounding)."""
+    rng = np.random.default_rng(3)
+    mant = 1.0 + rng.random(5000)
+    r = torch.from_numpy(np.where(rng.random(5000) < 0.5, -1, 1) * mant * np.exp2(rng.integers(0, 30, 5000)))
+    r = r.to(torch.bfloat16)
+    mag = r.abs()
+    up = (mag.view(torch.int16) + 1).view(torch.bfloat16).to(torch.float64).numpy()
+    step = up - mag.to(torch.float64).numpy()
+    tol = F.tolerance(r.to(torch.float64).numpy(), np.zeros(r.numel()))
+    assert np.all(tol >= step) and np.all(tol < 2 * step)
 
 
 def test_both_bf16_casts_match_torch():

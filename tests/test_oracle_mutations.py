@@ -115,6 +115,16 @@ PY_MUTANTS = [
      "w2e = w2[0:I]"),
     ("oracle.ffn", "test_ffn_oracle.py", "expert range one row short", "s, t = int(cs[e]), int(cs[e + 1])",
      "s, t = int(cs[e]), int(cs[e + 1]) - (1 if cs[e + 1] > cs[e] else 0)"),
+    ("oracle.ffn", "test_ffn_oracle.py", "error bound inflated", "absb[s:t] = np.abs(sw) @ np.abs(w2e)",
+     "absb[s:t] = 10 * (np.abs(sw) @ np.abs(w2e))"),
+    ("oracle.ffn", "test_ffn_oracle.py", "tolerance four bf16 steps", "return 2.0 ** -7 * np.abs(result)",
+     "return 2.0 ** -5 * np.abs(result)"),
+    ("oracle.ffn", "test_ffn_oracle.py", "tolerance without the sw term", "+ 1.1 * 2.0 ** -7 * absb",
+     "+ 0.0 * absb"),
+    ("oracle.route", "test_route_oracle.py", "scales gathered in token order", "pertoken_scale=xs[src_row],",
+     "pertoken_scale=xs[np.sort(src_row)],"),
+    ("oracle.route", "test_route_oracle.py", "bad ids not flagged", "flags=0 if bool(valid.all()) else BAD_EXPERT_ID,",
+     "flags=0,"),
 ]
 
 
