@@ -15,7 +15,7 @@ def pytest_configure(config):
     if spec:
         name, path = spec.split("=", 1)
         mod = importlib.import_module(name)
-        ns = {"__name__": name + "_mutant"}
+        ns = {"__name__": name + "_mutant", "__file__": mod.__file__}
         exec(compile(open(path).read(), path, "exec"), ns)
         for k, v in ns.items():
             if callable(v) and getattr(v, "__module__", None) == ns["__name__"]:

@@ -4,8 +4,9 @@ least one of its pins fail.
     dropped or misplaced term, a wrong sign, an off-by-one range, swapped nibbles): each mutant
     is built with the oracle's own compiler flags and run through test_oracle_pins.py in a
     child process (GMMFR_ORACLE_LIB points the oracle at it).
-  - The routing and FFN oracles (numpy): the pins of test_route_oracle.py / test_ffn_oracle.py
-    run in a child process whose conftest swaps in the functions of the mutated source
+  - The routing and FFN oracles (numpy) and the operator oracle's argument marshalling
+    (Python): the pins of test_route_oracle.py / test_ffn_oracle.py / test_oracle_pins.py run in
+    a child process whose conftest swaps in the functions of the mutated source
     (GMMFR_ORACLE_PY_MUTANT)."""
 import concurrent.futures as cf
 import os
@@ -125,11 +126,29 @@ PY_MUTANTS = [
      "pertoken_scale=xs[np.sort(src_row)],"),
     ("oracle.route", "test_route_oracle.py", "bad ids not flagged", "flags=0 if bool(valid.all()) else BAD_EXPERT_ID,",
      "flags=0,"),
+    # the operator oracle's argument marshalling (oracle/__init__.py)
+    ("oracle", "test_oracle_pins.py", "transpose flag dropped", "transpose_x2=int(bool(transpose_x2))",
+     "transpose_x2=0"),
+    ("oracle", "test_oracle_pins.py", "per-expert scale flag dropped", "scale_per_expert=int(bool(scale_per_expert))",
+     "scale_per_expert=0"),
+    ("oracle", "test_oracle_pins.py", "shared weight fixed at 1", "shared_weight=float(shared_weight)",
+     "shared_weight=1.0"),
+    ("oracle", "test_oracle_pins.py", "group_list read as counts", "group_list_type=int(group_list_type)",
+     "group_list_type=1"),
+    ("oracle", "test_oracle_pins.py", "logit not passed", 'logit=ptr(k["logit"])', "logit=None"),
+    ("oracle", "test_oracle_pins.py", "sampled rows and columns swapped",
+     "rows.size, rows.ctypes.data_as(ctypes.c_void_p),\n                                     cols.ctypes",
+     "rows.size, cols.ctypes.data_as(ctypes.c_void_p),\n                                     rows.ctypes"),
 ]
 
 
+def _module_path(module):
+    path = os.path.join(ROOT, *module.split("."))
+    return os.path.join(path, "__init__.py") if os.path.isdir(path) else path + ".py"
+
+
 def _py_pins_fail(tmp, i, module, pins, old, new):
-    src_path = os.path.join(ROOT, *module.split(".")) + ".py"
+    src_path = _module_path(module)
     src = open(src_path).read()
     assert src.count(old) == 1, old
     path = os.path.join(tmp, f"py{i}.py")
@@ -147,8 +166,9 @@ def test_every_planted_mistake_in_the_numpy_oracles_fails_a_pin(tmp_path):
     survivors = [m[2] for m, c in zip(PY_MUTANTS, caught) if not c]
     assert not survivors, f"mutants no pin catches: {survivors}"
     # the unmodified sources pass their pins by the same route
-    for module, pins in (("oracle.route", "test_route_oracle.py"), ("oracle.ffn", "test_ffn_oracle.py")):
-        path = os.path.join(ROOT, *module.split(".")) + ".py"
+    for module, pins in (("oracle.route", "test_route_oracle.py"), ("oracle.ffn", "test_ffn_oracle.py"),
+                         ("oracle", "test_oracle_pins.py")):
+        path = _module_path(module)
         env = dict(os.environ, GMMFR_ORACLE_PY_MUTANT=f"{module}={path}", OMP_NUM_THREADS="1")
         r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", pins), "-q",
                             "-p", "no:cacheprovider"], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
