@@ -75,11 +75,16 @@ def _pins_fail(lib):
     return r.returncode == 1 and " failed" in r.stdout
 
 
-def test_every_planted_mistake_fails_a_pin(tmp_path):
+@pytest.fixture(scope="module")
+def mutant_libs(tmp_path_factory):
     import oracle
     oracle.build()
-    # the unmodified source passes the pins through the same route
-    libs = [_build(str(tmp_path), i, old, new) for i, (_, old, new) in enumerate(MUTANTS)]
+    tmp = str(tmp_path_factory.mktemp("mutants"))
+    return [_build(tmp, i, old, new) for i, (_, old, new) in enumerate(MUTANTS)]
+
+
+def test_every_planted_mistake_fails_a_pin(mutant_libs):
+    libs = mutant_libs
     with cf.ThreadPoolExecutor(min(8, os.cpu_count() or 1)) as ex:
         caught = list(ex.map(_pins_fail, libs))
     survivors = [m[0] for m, c in zip(MUTANTS, caught) if not c]
@@ -181,3 +186,101 @@ def test_the_unmodified_source_passes_through_the_same_route(tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"), "-q",
                         "-p", "no:cacheprovider"], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-2000:]
+
+
+# ----------------------------------------------------------------------------- the parity tolerance
+# Mistakes whose effect the GPU parity comparison cannot see by construction: a doubled E5M2
+# subnormal moves a result far less than the bound allows (1e-4 of the sum of |products|), and
+# Inf / NaN decoding only shows on inputs holding those codes (pinned above, and by the NaN
+# placement parity test).
+_BELOW_TOLERANCE = {"E5M2 subnormal exponent", "E5M2 infinity read as NaN", "E8M0 NaN code read as a power of two"}
+
+
+def _cases():
+    """Small workloads of the GPU parity suite's kinds, with a bad row and a bad group_list."""
+    import torch
+
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+
+    base = dict(name="t", batch=16, M=40, K=256, N=320, E=4, seed=11)
+    kinds = [
+        dict(rows="random", shared_rows=6, shared_offset=5, shared_weight=0.7, out_init="randn"),
+        dict(transpose_x2=True, bias=True, rows="random"),
+        dict(x1_dtype=W.E5M2, x2_dtype=W.E5M2, group_list_type=0, scale_lo=120, scale_hi=134),
+        dict(scale_per_expert=True),
+        dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1),
+        dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, transpose_x2=True, K=352, N=200),
+    ]
+    out = []
+    for kw in kinds:
+        spec = W.Spec(**dict(base, **kw))
+        out.append((spec, W.make_inputs(spec)))
+    spec = W.Spec(**dict(base, rows="random"))
+    inp = W.make_inputs(spec)
+    inp["row_index"][3] = spec.batch                                   # a bad row
+    out.append((spec, inp))
+    spec = W.Spec(**dict(base, counts="explicit", explicit_counts=(10, 10, 10, 10)))
+    inp = W.make_inputs(spec)
+    inp["group_list"] = torch.tensor([12, 8, 10, 15], dtype=torch.int64)  # counts past M
+    out.append((spec, inp))
+    return out
+
+
+def _mutant_runs(lib_path, p, rows, cols):
+    import ctypes
+
+    import numpy as np
+
+    import oracle
+    lib = ctypes.CDLL(lib_path)
+    P = ctypes.POINTER(oracle._Args)
+    vp = ctypes.c_void_p
+    lib.oracle_gmmfr.argtypes = [P, vp, vp]
+    lib.oracle_gmmfr_sampled.argtypes = [P, ctypes.c_int64, vp, vp, vp, vp]
+    full = np.zeros((p.batch, p.N))
+    absb = np.zeros((p.batch, p.N))
+    flags = lib.oracle_gmmfr(ctypes.byref(p.args), full.ctypes.data_as(vp), absb.ctypes.data_as(vp))
+    vals = np.zeros(rows.size)
+    bnd = np.zeros(rows.size)
+    sflags = lib.oracle_gmmfr_sampled(ctypes.byref(p.args), rows.size, rows.ctypes.data_as(vp),
+                                      cols.ctypes.data_as(vp), vals.ctypes.data_as(vp), bnd.ctypes.data_as(vp))
+    return full, flags, vals, sflags
+
+
+def test_parity_tolerance_rejects_each_arithmetic_mistake(mutant_libs):
+    """The GPU parity tests accept a result within oracle.tolerance of the oracle and with the
+    same error flags.  Each planted mistake, if it were the kernel's, would fail that check on
+    at least one small workload of the kinds the GPU suite runs (the full comparison, or the
+    sampled one used at full size)."""
+    import numpy as np
+
+    import oracle
+
+    cases = []
+    for spec, inp in _cases():
+        p = oracle.problem_from_spec(spec, inp)
+        ref, absb, flags = oracle.run(p)
+        init = inp["out"].numpy().astype(np.float64)
+        sh = np.zeros_like(init)
+        if inp["shared_input"] is not None:
+            R = inp["shared_input"].shape[0]
+            sh[spec.shared_offset:spec.shared_offset + R] = (
+                spec.shared_weight * inp["shared_input"].float().numpy().astype(np.float64))
+        bound = oracle.tolerance(ref, absb, init, sh)
+        rr, cc = np.meshgrid(np.arange(spec.batch), np.arange(spec.N), indexing="ij")
+        cases.append((p, ref, flags, bound, rr.ravel().astype(np.int64), cc.ravel().astype(np.int64)))
+    unseen = []
+    for (name, _, _), lib in zip(MUTANTS, mutant_libs):
+        if name in _BELOW_TOLERANCE:
+            continue
+        seen = False
+        for p, ref, flags, bound, rows, cols in cases:
+            full, mflags, vals, sflags = _mutant_runs(lib, p, rows, cols)
+            bad_full = mflags != flags or not np.all(np.abs(full - ref) <= bound)
+            bad_sampled = sflags != flags or not np.all(np.abs(vals - ref.ravel()) <= bound.ravel())
+            if bad_full or bad_sampled:
+                seen = True
+                break
+        if not seen:
+            unseen.append(name)
+    assert not unseen, f"mistakes the parity tolerance accepts: {unseen}"
