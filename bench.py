@@ -27,7 +27,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "µs/call and achieved HBM GB/s vs roofline, MXFP8 grouped-matmul-finalize-routing"
-DEFAULT_CONFIG = 2
+DEFAULT_CONFIG = 5  # the large-E workload (M 4096, K 7168, N 4096, E 256): the largest that fits one GPU
 FMT_NAMES = {0: "E4M3", 1: "E5M2", 2: "E2M1"}
 # GPU sleep placed before each timed call, outside its events (about 0.5 ms at 2 GHz): the
 # device stays busy while the host enqueues the call, so the events time device work only
@@ -165,6 +165,23 @@ def _oracle_problem(spec, inp, ncols):
                           shared_offset=spec.shared_offset, shared_weight=spec.shared_weight, bias=bias)
 
 
+def _oracle_columns(spec, inp, seconds, probe=None):
+    """Output columns [0, ncols) that the oracle finishes in about `seconds` on this host
+    (multiples of 64; all N when the whole workload fits).  `probe` = (columns, seconds) of
+    an earlier run, else one is made here.  Returns (ncols, est. seconds for all N, probe)."""
+    import oracle
+    if probe is None:
+        cols = min(spec.N, 64 * max(1, oracle.num_threads()))
+        t0 = time.perf_counter()
+        oracle.run(_oracle_problem(spec, inp, cols))
+        probe = (cols, time.perf_counter() - t0)
+    est_full = probe[1] * spec.N / probe[0]
+    if est_full <= seconds:
+        return spec.N, est_full, probe
+    ncols = int(spec.N * seconds / max(est_full, 1e-9)) // 64 * 64
+    return min(spec.N, max(64, ncols)), est_full, probe
+
+
 def _cpu_baseline(spec, inp, min_s=10.0, max_s=30.0):
     """The oracle, as it stands, on all host cores: the whole workload (repeated
     until about min_s of work) when a probe predicts it takes at most max_s,
@@ -174,15 +191,12 @@ def _cpu_baseline(spec, inp, min_s=10.0, max_s=30.0):
     from moe_grouped_gemm_mxfp8_gb300 import workloads as W
 
     threads = oracle.num_threads()
-    probe_cols = min(spec.N, 64 * max(1, threads))
-    t0 = time.perf_counter()
-    oracle.run(_oracle_problem(spec, inp, probe_cols))
-    probe = time.perf_counter() - t0
-    est_full = probe * spec.N / probe_cols
-    if est_full <= max_s:
-        ncols, reps = spec.N, max(1, int(min_s / max(est_full, 1e-3)))
+    ncols, est_full, _ = _oracle_columns(spec, inp, max_s)
+    if ncols == spec.N:
+        reps = max(1, int(min_s / max(est_full, 1e-3)))
     else:
-        ncols, reps = min(spec.N, max(probe_cols, int(probe_cols * min_s / max(probe, 1e-3)) // 64 * 64)), 1
+        ncols, _, _ = _oracle_columns(spec, inp, min_s, (spec.N, est_full))
+        reps = 1
     p = _oracle_problem(spec, inp, ncols)
     t0 = time.perf_counter()
     for _ in range(reps):
@@ -194,29 +208,40 @@ def _cpu_baseline(spec, inp, min_s=10.0, max_s=30.0):
     return gbs, dt, f"oracle on {what}, {reps} run(s), {dt:.1f} s", threads
 
 
-def _profiled_traffic(workload, as_captured=True):
-    """DRAM bytes per gemm_kernel launch from the committed ncu summary of this
-    workload, if the kernel sources are unchanged since that capture and the run is set up
-    as it was (atomic mode, no bias, no tiling hint: `as_captured`); else None."""
-    if not as_captured:
-        return None
+PROFILE_RECORD = os.path.join(ROOT, "profiles", "gemm_kernel_traffic.json")
+KERNEL_SOURCES = ("kernels_gemm.cu", "ptx.cuh", "common.cuh", "pipeline.cuh")
+
+
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the grouped GEMM kernel's sources."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "gemm_kernel_" + workload.split()[0] + ".md")
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "moe_grouped_gemm_mxfp8_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_record(workload):
+    """The committed ncu record (profiles/gemm_kernel_traffic.json) of this workload: DRAM
+    bytes per gemm_kernel launch and the counters behind them, or None."""
     try:
-        text = open(path).read()
+        with open(PROFILE_RECORD) as f:
+            rec = json.load(f)
     except OSError:
         return None
-    h = hashlib.sha256()
-    for f in ("kernels_gemm.cu", "ptx.cuh", "common.cuh"):
-        h.update(open(os.path.join(ROOT, "moe_grouped_gemm_mxfp8_gb300", "csrc", f), "rb").read())
-    want = {}
-    for line in text.splitlines():
-        if ":" in line and line.strip().startswith(("source-sha256-16", "traffic-bytes-per-launch")):
-            k, v = line.strip().strip("`").split(":", 1)
-            want[k.strip()] = v.strip().strip("`")
-    if want.get("source-sha256-16") != h.hexdigest()[:16]:
+    return rec.get("workloads", {}).get(workload.split()[0])
+
+
+def _profiled_traffic(workload, as_captured=True):
+    """DRAM bytes per gemm_kernel launch from the committed ncu record of this workload, if
+    the kernel sources are unchanged since that capture and the run is set up as it was
+    (atomic mode, no bias, no tiling hint: `as_captured`); else None."""
+    if not as_captured:
         return None
-    return int(want["traffic-bytes-per-launch"]) if "traffic-bytes-per-launch" in want else None
+    r = profile_record(workload)
+    if r is None or r.get("source_sha256_16") != kernel_source_hash():
+        return None
+    return int(r["traffic_bytes_per_launch"])
 
 
 def _time_route(args, flush):
@@ -343,56 +368,138 @@ def _time_ffn(args, flush):
             "tflops": W.ffn_flops(fs) / (ms * 1e-3) / 1e12, "algorithmic_bytes": nbytes, "launches": 2}
 
 
-def _time_mxfp4(args, flush):
-    """Device time of the operator on MXFP4 inputs (E2M1 tokens and weights, E8M0 per
-    32) at the large shape (M 4096, K 7168, N 4096, E 256), against the algorithmic
-    bytes of the packed FP4 inputs.  Tokens and prepared weights stay packed (one GEMM
-    launch of kind::mxf4 MMAs)."""
+def _timed_calls(call, flush, steps, reset=None, clocks_index=None, world=1):
+    """`steps` steps of: L2 flush, reset() (restores out), a GPU sleep (so the host has
+    enqueued the call before the device reaches it), then call() between two CUDA events on
+    the current stream.  Returns (per-call ms, clock summary or None, wall seconds)."""
+    import torch
+    import torch.distributed as dist
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(clocks_index if clocks_index is not None else 0, enabled=clocks_index is not None) as clk:
+        t_wall = time.perf_counter()
+        for i in range(steps):
+            flush()
+            if reset is not None:
+                reset()
+            torch.cuda._sleep(SLEEP_CYCLES)
+            starts[i].record()
+            call()
+            ends[i].record()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], (clk.summary() if clocks_index is not None else None), t_wall
+
+
+def _kernel_breakdown(call, flush, steps, reset=None):
+    """The same steps again with the library's per-kernel events (which add a few
+    microseconds inside a call, so they stay out of the timed steps): per call, the ms of
+    each profile slot (-1 where the slot's kernel did not run)."""
+    import torch
+
+    from moe_grouped_gemm_mxfp8_gb300 import binding as B
+    B.gmmfr_profile_begin(steps)
+    for _ in range(steps):
+        flush()
+        if reset is not None:
+            reset()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        call()
+    return B.gmmfr_profile_end(steps)
+
+
+def _device_inputs(spec):
+    """Inputs of a workload on the device (the weights drawn there by a seeded CUDA generator)."""
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+    inp = W.make_inputs(spec, device="cpu", weights_device="cuda")
+    return inp, {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+
+
+def _measure(spec, deterministic, flush, steps, warmup, d=None, prep=None):
+    """Device time of one call on a workload (atomic or deterministic mode), with the GEMM
+    kernel's share from a profiled pass; algorithmic bytes over the time as GB/s and as a
+    fraction of the measured copy bandwidth."""
     import torch
 
     from moe_grouped_gemm_mxfp8_gb300 import binding as B
     from moe_grouped_gemm_mxfp8_gb300 import workloads as W
 
-    spec = W.mxfp4_config()
-    inp = W.make_inputs(spec, weights_device="cuda")
-    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
-    prob = B.problem_from_spec(spec)
-    prep = B.prepare_weights(prob, d["x2"], d["scale"])
-    del d["x2"]
+    if d is None:
+        _, d = _device_inputs(spec)
+    prob = B.problem_from_spec(spec, deterministic)
+    if prep is None:
+        prep = B.prepare_weights(prob, d["x2"], d["scale"])
     ws = B.workspace(prob, True, "cuda")
     out = d["out"].clone()
-    for _ in range(args.warmup):
+
+    def call():
         B.run(prob, d, out, prepared=prep, ws=ws)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for e0, e1 in ev:  # timed: one event pair around each call
-        flush()
-        torch.cuda._sleep(SLEEP_CYCLES)
-        e0.record()
-        B.run(prob, d, out, prepared=prep, ws=ws)
-        e1.record()
-    torch.cuda.synchronize()
-    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
-    B.gmmfr_profile_begin(args.steps)  # per-kernel breakdown, a second pass
-    for _ in range(args.steps):
-        flush()
-        torch.cuda._sleep(SLEEP_CYCLES)
-        B.run(prob, d, out, prepared=prep, ws=ws)
-    k = B.gmmfr_profile_end(args.steps)
+
+    def reset():
+        out.copy_(d["out"])
+
+    for _ in range(warmup):
+        call()
+    call_ms, _, _ = _timed_calls(call, flush, steps, reset)
+    k = _kernel_breakdown(call, flush, steps, reset)
     bits = B.gmmfr_check_device_errors(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
     nbytes = W.algorithmic_bytes(spec)
-    peaks, _ = _peaks()
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    del prep, ws
-    expand = [x[0] for x in k if x[0] is not None and x[0] >= 0]  # slot 0: E2M1 token expansion, when it runs
-    return {"workload": spec.name, "us_per_call": ms * 1e3, "gbs": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"]),
-            "expand_us": statistics.mean(expand) * 1e3 if expand else None,
-            "gemm_us": statistics.mean(x[2] for x in k) * 1e3,
-            "tflops": W.flops(spec) / (ms * 1e-3) / 1e12, "algorithmic_bytes": nbytes, "launches": 2 if expand else 1,
-            "device_error_bits": bits}
+    hbm = float(_peaks()[0]["hbm_gbs"])
+    ms = statistics.mean(call_ms)
+    gemm_ms = statistics.mean(x[2] for x in k)
+    comb = [x[3] for x in k if x[3] >= 0]
+    return {"workload": spec.name, "mode": "deterministic" if deterministic else "atomic",
+            "us_per_call": ms * 1e3, "us_per_call_p10_p50_p90": [round(float(x) * 1e3, 2) for x in _quantiles(call_ms, (0.1, 0.5, 0.9))],
+            "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+            "gemm_us": gemm_ms * 1e3, "gemm_frac_hbm": nbytes / (gemm_ms * 1e-3) / 1e9 / hbm,
+            "combine_us": statistics.mean(comb) * 1e3 if comb else None,
+            "tflops": W.flops(spec) / (ms * 1e-3) / 1e12, "algorithmic_bytes": nbytes,
+            "launches_per_call": sum(1 for s in (0, 1, 2, 3) if k[0][s] >= 0), "device_error_bits": bits}
+
+
+def _time_mxfp4(args, flush):
+    """Device time of the operator on MXFP4 inputs (E2M1 tokens and weights, E8M0 per
+    32) at the large shape (M 4096, K 7168, N 4096, E 256), against the algorithmic
+    bytes of the packed FP4 inputs.  Tokens and prepared weights stay packed (one GEMM
+    launch of kind::mxf4 MMAs)."""
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+    return _measure(W.mxfp4_config(), False, flush, args.steps, args.warmup)
+
+
+def _sub_workloads(args, flush, main_spec, d, prep):
+    """Every other benchmark workload, one line each: the four smaller configs in atomic
+    mode, and the deterministic mode on the second, fourth and largest (the largest reusing
+    the timed call's inputs and prepared weights)."""
+    import torch
+
+    from moe_grouped_gemm_mxfp8_gb300 import workloads as W
+    res = {}
+    for i in (1, 2, 3, 4):
+        spec = W.config(i)
+        if spec.name == main_spec.name:
+            continue
+        _, di = _device_inputs(spec)
+        res[spec.name.split()[0]] = _measure(spec, False, flush, args.steps, args.warmup, d=di)
+        if i in (2, 4):
+            res[spec.name.split()[0] + " deterministic"] = _measure(spec, True, flush, args.steps, args.warmup, d=di)
+        del di
+        torch.cuda.empty_cache()
+    if main_spec.name == W.config(5).name:
+        res["C5 deterministic"] = _measure(main_spec, True, flush, args.steps, args.warmup, d=d, prep=prep)
+    return res
 
 
 def run_reference(args):
-    """The oracle (CPU) as the reference arm: each step is a bounded column sample."""
+    """The oracle (CPU) as the reference arm, on the same workload and input bytes as the
+    GPU arm (the weights drawn by the same seeded CUDA generator, then copied to the host).
+    Each step runs the oracle on a bounded sample, output columns [0, ncols) of the workload,
+    sized so that all warm-up and timed steps take about two and a half minutes; its rate is
+    scaled to the whole workload by N / ncols."""
     import torch
 
     from moe_grouped_gemm_mxfp8_gb300 import workloads as W
@@ -400,36 +507,49 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import oracle
     spec = _main_spec(args)
-    inp = W.make_inputs(spec)
+    inp = W.make_inputs(spec, device="cpu", weights_device="cuda" if torch.cuda.is_available() else "cpu")
+    inp["x2"] = inp["x2"].cpu()
+    torch.cuda.empty_cache() if torch.cuda.is_available() else None
     counts = W.expert_counts(spec)
+    per_step = min(10.0, max(1.0, 150.0 / max(1, args.warmup + args.steps)))
+    ncols, est_full, _ = _oracle_columns(spec, inp, per_step)
+    p = _oracle_problem(spec, inp, ncols)
+    nbytes = W.algorithmic_bytes(spec)
     vals = []
-    sample = ""
-    cores = 1
     for i in range(args.warmup + args.steps):
-        gbs, dt, sample, cores = _cpu_baseline(spec, inp)
+        t0 = time.perf_counter()
+        oracle.run(p)
+        dt = (time.perf_counter() - t0) * spec.N / ncols
         if i >= args.warmup:
-            vals.append(gbs)
+            vals.append(nbytes / dt / 1e9)
     v = statistics.median(vals)
-    full_ms = W.algorithmic_bytes(spec) / (v * 1e9) * 1e3
+    full_ms = nbytes / (v * 1e9) * 1e3
+    sample = (f"oracle on output columns [0,{ncols}) of {spec.N} per step (whole workload ~{est_full:.1f} s on "
+              f"{oracle.num_threads()} threads), rate scaled by N/{ncols}")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config_dict(spec, counts, args.deterministic),
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def _main_spec(args):
-    """The workload of the timed call: --config N, or with --fp4 the MXFP4 operator at the
-    large shape (c5) or its reduced copy (e32); --bias adds the per-expert bf16 bias."""
+    """The workload of the timed call: --config N (with --e32 the 32-expert copy of the large
+    workload, for full profiler captures), or with --fp4 the MXFP4 operator at the large
+    shape (c5) or its reduced copy (e32); --bias adds the per-expert bf16 bias."""
     from moe_grouped_gemm_mxfp8_gb300 import workloads as W
 
     if args.fp4 == "c5":
         spec = W.mxfp4_config()
     elif args.fp4 == "e32":
         spec = W.mxfp4_small_config()
+    elif args.e32:
+        spec = W.large_small_config()
     else:
         spec = W.config(args.config)
     if args.bias:
@@ -458,8 +578,7 @@ def run_ours(args):
     counts = W.expert_counts(spec)
     alg_bytes = W.algorithmic_bytes(spec, counts)
     flops = W.flops(spec, counts)
-    inp = W.make_inputs(spec, device="cpu", weights_device="cuda")
-    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    inp, d = _device_inputs(spec)
     prob = B.problem_from_spec(spec, args.deterministic)
     prob.expected_tokens_per_expert = args.tokens_hint  # the tuning hint (0: chosen on the device)
     stream = torch.cuda.current_stream()
@@ -480,47 +599,21 @@ def run_ours(args):
     out = d["out"].clone()
     flush = L2Flush()
 
-    def call(o):
-        B.run(prob, d, o, prepared=prep, ws=ws)
+    def call():
+        B.run(prob, d, out, prepared=prep, ws=ws)
+
+    def reset():
+        out.copy_(out0)
 
     for _ in range(args.warmup):
-        call(out)
+        call()
     torch.cuda.synchronize()
     bits = B.gmmfr_check_device_errors(ws.data_ptr(), sptr)
 
-    sleep_cycles = SLEEP_CYCLES
-
-    def timed_steps(n, with_clocks):
-        """n steps of: L2 flush, reset of out, a GPU sleep (so the host has enqueued the
-        call before the device reaches it), then the call between two CUDA events."""
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        with ClockSampler(local, enabled=with_clocks) as clk:
-            t_wall = time.perf_counter()
-            for i in range(n):
-                flush()
-                out.copy_(out0)
-                torch.cuda._sleep(sleep_cycles)
-                starts[i].record()
-                call(out)
-                ends[i].record()
-            torch.cuda.synchronize()
-            t_wall = time.perf_counter() - t_wall
-        if world > 1:
-            dist.barrier()
-        return [a.elapsed_time(b) for a, b in zip(starts, ends)], clk, t_wall
-
     # the timed steps: nothing but the call between the events
-    call_ms, clk, t_wall = timed_steps(args.steps, True)
+    call_ms, clocks, t_wall = _timed_calls(call, flush, args.steps, reset, clocks_index=local, world=world)
     ms = reduce_step_time(statistics.mean(call_ms), world)
-    # the same steps again with the library's per-kernel events, for the kernel breakdown
-    # (the extra events inside a call add a few microseconds, so they are kept out of the timed steps)
-    B.gmmfr_profile_begin(args.steps)
-    prof_ms, _, _ = timed_steps(args.steps, False)
-    kernel_ms = B.gmmfr_profile_end(args.steps)
+    kernel_ms = _kernel_breakdown(call, flush, args.steps, reset)
     gemm_ms = statistics.mean(k[2] for k in kernel_ms)
     # kernels of one call, from the slots the profiled pass saw run (input preparation, GEMM,
     # deterministic combine)
@@ -602,6 +695,7 @@ def run_ours(args):
     t_end.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = t_start.elapsed_time(t_end) / args.steps
+    del sets, dev_buf, dd
 
     peaks, peak_kind = _peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -624,6 +718,7 @@ def run_ours(args):
                      "frac": gemm_gbs / hbm_peak, "traffic": _profiled_traffic(
                          spec.name, not (args.deterministic or spec.bias or args.tokens_hint)),
                      "kernel": "gemm_kernel (grouped GEMM + fused epilogue)",
+                     "achieved_how": "algorithmic bytes / mean gemm_kernel duration (CUDA events on the call's stream, profiled pass)",
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
         "e2e": {"value": alg_bytes / (e2e_serial_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_serial_ms,
@@ -632,15 +727,19 @@ def run_ours(args):
                 "pipelined_mode": "copy in, call and copy out of consecutive steps overlap on three streams"},
         "gpu_launches": args.steps * launches_per_call,
         "device_error_bits": bits,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "wall_s_timed": t_wall,
     }
     if not args.no_extras:
+        line["configs"] = _sub_workloads(args, flush, spec, d, prep)
         line["route"] = _time_route(args, flush)
         if W.route_config(args.config).M == spec.M:
             line["layer"] = _time_layer(args, flush, prob, d, prep, ws, ms * 1e3, line["route"]["us_per_call"])
         line["ffn"] = _time_ffn(args, flush)
-        line["mxfp4"] = _time_mxfp4(args, flush)
+        if spec.x1_dtype != W.E2M1:
+            del prep
+            torch.cuda.empty_cache()
+            line["mxfp4"] = _time_mxfp4(args, flush)
     if rank == 0 and not args.no_cpu_baseline:
         cgbs, cdt, sample, cores = _cpu_baseline(spec, inp)
         line["cpu_baseline"] = {"value": cgbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
@@ -658,6 +757,8 @@ def main():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--fp4", default="off", choices=["off", "c5", "e32"],
                     help="time the MXFP4 (E2M1) operator instead: the large shape, or its 32-expert copy")
+    ap.add_argument("--e32", action="store_true",
+                    help="time the 32-expert copy of the large workload (for full profiler captures)")
     ap.add_argument("--bias", action="store_true", help="add the per-expert bf16 bias input")
     ap.add_argument("--tokens-hint", type=int, default=0,
                     help="expected_tokens_per_expert tuning hint (fixes the token group width)")
@@ -665,7 +766,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the side measurements (routing step, SwiGLU FFN, MXFP4 operator)")
+                    help="skip the side measurements (the other workloads, routing step, SwiGLU FFN, MXFP4 operator)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

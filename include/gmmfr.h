@@ -209,18 +209,28 @@ GMMFR_API gmmfr_status gmmfr_check_device_errors(const void* workspace, void* st
  *              them itself); other arguments as for the operator.
  * Problems whose workspace (gmmfr_workspace_size with have_prepared = 1) exceeds
  * 16 MiB are rejected with GMMFR_ERR_WORKSPACE and a message giving both sizes.
- * The first call on each device resolves the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  All calls share the one array and it keeps the last call's
- * contents (the operator rewrites every word it reads, so nothing needs
- * clearing); calls that can overlap on the GPU (different streams, or several
- * host threads) race on it and must be serialised by the caller.  The device
- * error word of these calls lives in that array and is not exposed.
+ * Outside stream capture each call looks up the array's device address on the current
+ * device (cudaGetSymbolAddress, with that device current), so the address stays right
+ * after the device's context is destroyed and re-created.  Inside a capture the address
+ * found by an earlier call on the device is used: make one call on each device before
+ * any stream capture; a first call inside a capture returns GMMFR_ERR_UNSUPPORTED.
+ * All calls share the one array and it keeps the last call's contents (the operator
+ * rewrites every word it reads, so nothing needs clearing); calls that can overlap on
+ * the GPU (different streams, or several host threads) race on it and must be
+ * serialised by the caller.
  */
 GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing_static_scratch(
     const gmmfr_problem* problem, const void* x1, const void* pertoken_scale, const int64_t* group_list,
     const float* logit, const void* row_index, const void* shared_input, float* out, const void* prepared,
     void* stream);
+
+/*
+ * gmmfr_check_device_errors for the allocation-free entry point: SYNCHRONISES `stream`,
+ * then reads the device error word that the last static-scratch call on the current
+ * device left in the library's scratch array (GMMFR_DEV_* bits) into *bits.  Returns
+ * GMMFR_ERR_DEVICE when any bit is set, GMMFR_OK otherwise.
+ */
+GMMFR_API gmmfr_status gmmfr_static_scratch_check_device_errors(void* stream, uint32_t* bits);
 
 /*
  * The routing step before the operator (LLaDA2.0-mini grouped-GEMM write-up,

@@ -29,6 +29,7 @@ ENTRY_POINTS = (
     "gmmfr_prepared_weights_size", "gmmfr_prepare_weights", "gmmfr_workspace_size",
     "gmmfr_grouped_matmul_finalize_routing", "gmmfr_check_device_errors", "gmmfr_last_error",
     "gmmfr_profile_begin", "gmmfr_profile_end", "gmmfr_grouped_matmul_finalize_routing_static_scratch",
+    "gmmfr_static_scratch_check_device_errors",
     "gmmfr_moe_route_workspace_size", "gmmfr_moe_route",
     "gmmfr_ffn_prepared_weights_size", "gmmfr_ffn_prepare_weights", "gmmfr_ffn_workspace_size",
     "gmmfr_llada2_moe_grouped_gemm",
@@ -88,6 +89,7 @@ def load(path: str = LIB_PATH):
             lib.gmmfr_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
             lib.gmmfr_grouped_matmul_finalize_routing.argtypes = [P] + [vp] * 12 + [sz, vp]
             lib.gmmfr_grouped_matmul_finalize_routing_static_scratch.argtypes = [P] + [vp] * 9
+            lib.gmmfr_static_scratch_check_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
             RP = ctypes.POINTER(RouteProblem)
             lib.gmmfr_moe_route_workspace_size.argtypes = [RP, ctypes.POINTER(sz)]
             lib.gmmfr_moe_route.argtypes = [RP] + [vp] * 11 + [sz, vp]
@@ -172,6 +174,16 @@ def gmmfr_grouped_matmul_finalize_routing_static_scratch(problem: Problem, x1, p
     _check(load().gmmfr_grouped_matmul_finalize_routing_static_scratch(
         ctypes.byref(problem), x1, pertoken_scale, group_list, logit, row_index, shared_input, out, prepared,
         stream))
+
+
+def gmmfr_static_scratch_check_device_errors(stream=None) -> int:
+    """Synchronises `stream`; returns the device error bits of the last static-scratch call
+    on the current device (0 when clean)."""
+    bits = ctypes.c_uint32()
+    st = load().gmmfr_static_scratch_check_device_errors(stream, ctypes.byref(bits))
+    if st not in (OK, ERR_DEVICE):
+        _check(st)
+    return bits.value
 
 
 def gmmfr_moe_route_workspace_size(problem: RouteProblem) -> int:

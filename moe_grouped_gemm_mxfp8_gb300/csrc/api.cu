@@ -84,6 +84,21 @@ int device_sms() {
   return sms;
 }
 
+// Testing aids for the deterministic mode's schedule: GMMFR_GRID = the grouped GEMM's CTA count
+// (1 .. 1023; default one per SM), GMMFR_REVERSE_UNITS = 1 makes each CTA walk its units last to
+// first.  Neither changes the K split, so neither may change a bit of the result.
+int grid_override() {
+  if (const char* s = std::getenv("GMMFR_GRID")) {
+    const int v = std::atoi(s);
+    if (v >= 1 && v <= gmmfr::kMaxErrSlots) return v;
+  }
+  return 0;
+}
+bool reverse_units() {
+  const char* s = std::getenv("GMMFR_REVERSE_UNITS");
+  return s && std::atoi(s) != 0;
+}
+
 // Token group width fixed by the caller for tests (GMMFR_TMAX = 32, 64 or 128); 0 lets the
 // kernel pick the smallest width that holds the largest expert.
 int fixed_tmax() {
@@ -360,8 +375,10 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
     gp.test_stall = 1;
     gp.timeout_ns = std::atoll(t) > 0 ? std::atoll(t) : 1000000;
   }
+  gp.reverse_units = reverse_units();
+  const int grid = grid_override() ? grid_override() : std::min(sms, gmmfr::kMaxErrSlots);
   timer.begin(2, s);
-  e = gmmfr::launch_gemm(tmaps, gp, std::min(sms, gmmfr::kMaxErrSlots), s);
+  e = gmmfr::launch_gemm(tmaps, gp, grid, s);
   timer.end(2, s);
   if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
 

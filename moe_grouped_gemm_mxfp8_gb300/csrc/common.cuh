@@ -76,6 +76,7 @@ struct GemmParams {
   uint32_t idesc;          // instruction descriptor without N and scale-factor ids
   int64_t timeout_ns;
   int32_t test_stall;      // testing aid: wait on a barrier nothing arrives on
+  int32_t reverse_units;   // testing aid (deterministic mode): each CTA walks its units last to first
 };
 
 struct CombineParams {

@@ -170,7 +170,7 @@ struct Sched {
   int NT, KB, split, ng;
   bool det;
   int cur_g, cur_j, cur_kb;  // group, column tile and K block of item i (deterministic: K split)
-  __device__ void init(int n_groups, int NT_, int KB_, bool det_, int split_, const Groups& gr) {
+  __device__ void init(int n_groups, int NT_, int KB_, bool det_, int split_, bool reverse, const Groups& gr) {
     ng = n_groups;
     NT = NT_;
     KB = KB_;
@@ -179,13 +179,16 @@ struct Sched {
     const int64_t tiles = (int64_t)n_groups * NT;
     if (det) {
       // contiguous ranges of (group, tile, K split) units: unit u = tile * split + sp, walked
-      // from the first without dividing (cur_kb holds sp)
+      // from the first without dividing (cur_kb holds sp), or from the last when `reverse`
+      // (every unit writes its own slice of the per-token buffer, so the order in which a CTA
+      // takes its units cannot change the result; tests walk both ways)
       const int64_t units = tiles * split;
       i = units * blockIdx.x / gridDim.x;
       i_end = units * (blockIdx.x + 1) / gridDim.x;
-      step = 1;
-      const int64_t tile = i / split;
-      cur_kb = (int)(i - tile * split);
+      step = reverse ? -1 : 1;
+      const int64_t first = reverse && i_end > i ? i_end - 1 : i;
+      const int64_t tile = first / split;
+      cur_kb = (int)(first - tile * split);
       cur_g = (int)(tile % (ng > 0 ? ng : 1));
       cur_j = (int)(tile / (ng > 0 ? ng : 1));
       return;
@@ -238,11 +241,19 @@ struct Sched {
       s.kb1 = (int)((int64_t)(sp + 1) * KB / split);
       s.slot = sp;
       ++i;
-      if (++cur_kb == split) {
-        cur_kb = 0;
-        if (++cur_g == ng) {
-          cur_g = 0;
-          ++cur_j;
+      if (step > 0) {
+        if (++cur_kb == split) {
+          cur_kb = 0;
+          if (++cur_g == ng) {
+            cur_g = 0;
+            ++cur_j;
+          }
+        }
+      } else if (--cur_kb < 0) {
+        cur_kb = split - 1;
+        if (--cur_g < 0) {
+          cur_g = ng - 1;
+          --cur_j;
         }
       }
       return true;
@@ -527,7 +538,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
   const int off_xsf = cfg::off_xsf(fp4), off_x = cfg::off_x(fp4);
   const Ctl ctl{abort_flag, s_err, p.timeout_ns};
   Sched sched;
-  sched.init(n_groups, p.NT, p.KB, det, p.split, groups);
+  sched.init(n_groups, p.NT, p.KB, det, p.split, det && p.reverse_units, groups);
   const uint32_t smem_base = ptx::smem_u32(smem);
 
   if (warp == 0) {

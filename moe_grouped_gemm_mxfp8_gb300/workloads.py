@@ -246,6 +246,14 @@ def mxfp4_small_config() -> Spec:
                 rows="topk", topk=8, logit="softmax", x1_dtype=E2M1, x2_dtype=E2M1, seed=1106)
 
 
+def large_small_config() -> Spec:
+    """A reduced copy of the large MXFP8 workload (5): the same K, N, tokens per expert and
+    routing recipe with 32 experts (about 0.97 GB of prepared weights), sized for full
+    profiler captures; its traffic scales to the large workload by the expert count."""
+    return Spec("C5-E32 M512 K7168 N4096 E32", batch=64, M=512, K=7168, N=4096, E=32, counts="multinomial",
+                rows="topk", topk=8, logit="softmax", seed=1006)
+
+
 def algorithmic_bytes(spec: Spec, counts: Optional[torch.Tensor] = None) -> int:
     """Bytes a single call must move at minimum: x2 (and its scales) of every
     expert that holds a token, x1, pertoken_scale, logit, row_index,

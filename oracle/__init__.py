@@ -193,12 +193,11 @@ def num_threads() -> int:
     return _load().oracle_num_threads()
 
 
-def tolerance(out64: np.ndarray, absb: np.ndarray, out_init=None, shared_term=None) -> np.ndarray:
-    """Per-element bound |gpu - oracle| <= 1e-4*absb + 1e-6 (+ FP32 rounding of
-    the initial value and the shared term, 2^-20 of their magnitude)."""
-    b = 1e-4 * absb + 1e-6
-    if out_init is not None:
-        b = b + np.abs(out_init) * 2.0 ** -20
-    if shared_term is not None:
-        b = b + np.abs(shared_term) * 2.0 ** -20
-    return b
+def tolerance(out64: np.ndarray, absb: np.ndarray) -> np.ndarray:
+    """Per-element parity bound |gpu - oracle| <= 1e-4 * absb + 1e-6, where absb sums
+    |logit| * sum_k |a_k b_k| over the element's tokens: for an element with one token this
+    is the operator's stated accuracy bound 1e-4 * |logit| * sum_k |a_k b_k| + 1e-6, and
+    over several tokens each one's share of it.  The 1e-6 absolute term also covers the
+    FP32 rounding of the initial value and the shared term (about 2^-24 of |out|), which
+    keeps below it for |out| up to about 8."""
+    return 1e-4 * absb + 1e-6

@@ -20,3 +20,15 @@ def pytest_configure(config):
         for k, v in ns.items():
             if callable(v) and getattr(v, "__module__", None) == ns["__name__"]:
                 setattr(mod, k, v)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Largest err/bound of each GPU parity comparison (tests/_parity_report.py)."""
+    rep = sys.modules.get("_parity_report")
+    if rep is None or not rep.RATIOS:
+        return
+    terminalreporter.write_sep("-", "parity: max |gpu - oracle| / (1e-4 * absb + 1e-6)")
+    for k in sorted(rep.RATIOS):
+        terminalreporter.write_line(f"{rep.RATIOS[k]:.4f}  {k}")
+    terminalreporter.write_line(f"overall max {max(rep.RATIOS.values()):.4f} over {len(rep.RATIOS)} comparisons")
+    rep.write()
