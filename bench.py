@@ -590,7 +590,7 @@ def run_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(2):
         e0.record()
-        B.gmmfr_prepare_weights(prob, d["x2"].data_ptr(), d["scale"].data_ptr(), prep.data_ptr(), n_prep, sptr)
+        B.gmmfr_prepare_weights(prob, B.view(d["x2"]), B.view(d["scale"]), prep.data_ptr(), n_prep, sptr)
         e1.record()
     torch.cuda.synchronize()
     prep_ms = e0.elapsed_time(e1)

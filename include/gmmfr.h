@@ -15,8 +15,10 @@
  * scales by 32 along K, section 6.3).
  *
  * Conventions for every entry point:
- *   - Tensor arguments are DEVICE pointers to dense row-major data owned by the
- *     caller; the library keeps no pointer after a call returns.
+ *   - Tensor arguments are DEVICE memory owned by the caller, dense and row-major:
+ *     views (gmmfr_tensor, checked against the problem) for the operator and the
+ *     weight preparation, plain pointers for the routing step and the FFN, whose
+ *     problem structs give every size; the library keeps no pointer after a call returns.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Work is enqueued on it; no entry point synchronises unless it says so.
  *   - A call that returns an error status enqueues no work.  The message of the
@@ -43,7 +45,7 @@ extern "C" {
 typedef enum {
   GMMFR_OK = 0,
   GMMFR_ERR_INVALID_ARG = 1, /* a size, pointer, dtype code or offset is out of range */
-  GMMFR_ERR_UNSUPPORTED = 2, /* valid for the operator but not handled here (e.g. K % 16 != 0) */
+  GMMFR_ERR_UNSUPPORTED = 2, /* valid for the operator but not handled here (e.g. a first static-scratch call inside a capture) */
   GMMFR_ERR_WORKSPACE = 3,   /* workspace or prepared buffer too small or misaligned */
   GMMFR_ERR_CUDA = 4,        /* a CUDA runtime call failed (no device, launch error, ...) */
   GMMFR_ERR_DEVICE = 5       /* a device-side check failed; see gmmfr_check_device_errors */
@@ -73,11 +75,51 @@ typedef enum { GMMFR_INDEX_I64 = 0, GMMFR_INDEX_I32 = 1 } gmmfr_index_type;
 #define GMMFR_DEV_BAD_EXPERT_ID 8u  /* routing: a top-k expert id outside [0, E); that entry was routed nowhere */
 
 /*
+ * Tensor views.  Every tensor argument of the operator is passed as a non-owning view of
+ * dense device memory, so that the library can refuse a tensor whose rank, shape, element
+ * type or layout does not match the problem (as the aclnn operator checks its aclTensor
+ * arguments, "参数说明" / "约束说明") before anything is enqueued, instead of reading past
+ * its end.
+ *   data     device address; NULL only for a tensor with no elements
+ *   dtype    gmmfr_dtype.  FP8, E2M1 and E8M0 tensors may also be passed as raw bytes
+ *            (GMMFR_DT_U8); the problem's formats say how the bytes are read
+ *   ndim     1 .. 4
+ *   shape    in elements of dtype; packed E2M1 (GMMFR_DT_E2M1X2, or U8 holding E2M1 codes)
+ *            counts bytes, i.e. pairs of codes, along its packed dimension
+ *   strides  in elements; only dense row-major layouts are accepted (the last stride 1,
+ *            each other stride the product of the sizes after it; a dimension of size 1
+ *            may have any stride)
+ * A NULL view pointer means the tensor is absent (an optional input, or x2 and scale when
+ * prepared weights are given).
+ */
+typedef enum {
+  GMMFR_DT_U8 = 0,     /* raw bytes */
+  GMMFR_DT_E4M3 = 1,   /* FP8 E4M3FN */
+  GMMFR_DT_E5M2 = 2,   /* FP8 E5M2 */
+  GMMFR_DT_E2M1X2 = 3, /* two FP4 E2M1 codes per byte, the even element in the low nibble */
+  GMMFR_DT_E8M0 = 4,   /* E8M0 scale bytes, 2^(b-127) */
+  GMMFR_DT_I64 = 5,
+  GMMFR_DT_I32 = 6,
+  GMMFR_DT_F32 = 7,
+  GMMFR_DT_BF16 = 8
+} gmmfr_dtype;
+
+#define GMMFR_MAX_DIMS 4
+typedef struct {
+  void* data;
+  int32_t dtype;
+  int32_t ndim;
+  int64_t shape[GMMFR_MAX_DIMS];
+  int64_t strides[GMMFR_MAX_DIMS];
+} gmmfr_tensor;
+
+/*
  * Sizes, formats and scalar arguments of one call (section 3.1 tensor table and
  * section 5.1 FinalizeRoutingConfig fields).
  *
  *   M      rows of x1, pertoken_scale, logit, row_index (routed tokens, batch*topk); M >= 0
- *   K      contraction length, K >= 1 and K % 16 == 0
+ *   K      contraction length, K >= 1; even when E2M1 codes are packed along K (an E2M1 x1,
+ *          or a transposed E2M1 x2)
  *   N      output columns, N >= 0
  *   E      experts, 1 <= E <= 1024 (aclnn V3 constraint "e <= 1024")
  *   batch  rows of out, batch >= 0
@@ -129,38 +171,50 @@ GMMFR_API gmmfr_status gmmfr_prepared_weights_size(const gmmfr_problem* problem,
  * keeps the codes packed: 128 columns x 256 K (K pairs per byte, the lower K in the low
  * nibble) and then 1024 scale bytes (eight per row, in two 512-byte halves); otherwise
  * the E2M1 codes are stored prepared as E4M3 codes.
+ *   x2, scale       views with the shapes above (checked as for the operator)
  *   prepared        device buffer of at least gmmfr_prepared_weights_size bytes,
  *                   16-byte aligned, caller-owned; fully overwritten.
  * Enqueued on `stream`; the buffer stays valid as long as the caller keeps it.
  */
-GMMFR_API gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const void* x2, const void* scale,
-                                   void* prepared, size_t prepared_bytes, void* stream);
+GMMFR_API gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const gmmfr_tensor* x2,
+                                             const gmmfr_tensor* scale, void* prepared, size_t prepared_bytes,
+                                             void* stream);
 
 /*
  * Workspace bytes one call needs (two-phase use as in aclnn's
  * GetWorkspaceSize/execute pair).  `have_prepared` = 0 adds room to prepare
  * the weights inside the call; an E2M1 x1 that is expanded (x2 not E2M1, or
- * K % 32 != 0) adds M*K bytes for its expansion to E4M3.  Host only; may query the current device's SM count.  The workspace
- * must be 256-byte aligned.
+ * K % 32 != 0) adds M*K bytes for its expansion to E4M3, and x1 rows whose K is not a
+ * multiple of 16 add M*Kp bytes (Kp = K rounded up to 16) for a copy at a 16-byte pitch
+ * (the tensor copies that feed the GEMM need one).  Host only.  The workspace must be
+ * 256-byte aligned.
  */
 GMMFR_API gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int have_prepared, size_t* bytes);
 
 /*
  * The operator.  Enqueues the whole computation on `stream`; never syncs and
- * never allocates.
- *   x1              [M,K] FP8 bytes (E2M1: [M,K/2], two codes per byte), 16-byte aligned
- *   x2, scale       raw weights and their scales; read only when prepared == NULL
- *                   (they are then prepared into the workspace first)
- *   pertoken_scale  [M,ceil(K/64),2] E8M0 bytes
- *   group_list      [E] int64 (type per problem.group_list_type); checked on the device
+ * never allocates.  Every view is checked against the problem first: a tensor of the wrong
+ * rank, shape or element type, a layout that is not dense row-major, a missing required
+ * tensor, or a buffer smaller than its stated size is refused with GMMFR_ERR_INVALID_ARG
+ * (GMMFR_ERR_WORKSPACE for `prepared` and `workspace`) and nothing is enqueued.
+ *   x1              [M,K] FP8 (E4M3 / E5M2 per x1_format; E2M1: [M,K/2] E2M1X2), required
+ *                   when M > 0; 16-byte aligned when the GEMM reads it in place (FP8 codes,
+ *                   or E2M1 tokens and weights kept packed, with K % 16 == 0)
+ *   x2, scale       raw weights [E,K,N] / [E,N,K] and scales [(E,)ceil(K/64),N,2] /
+ *                   [(E,)N,ceil(K/64),2] (E8M0); read only when prepared == NULL (they are
+ *                   then prepared into the workspace first), and may be NULL otherwise
+ *   pertoken_scale  [M,ceil(K/64),2] E8M0, required when M > 0
+ *   group_list      [E] int64 (type per problem.group_list_type); values checked on the device
  *   logit           [M] float32, or NULL for weight 1 (has_logit = False)
- *   row_index       [M] int64 or int32; values in [0,batch), checked on the device
- *   shared_input    [shared_rows,N] bfloat16, or NULL when shared_rows == 0
+ *   row_index       [M] int64 or int32 (problem.row_index_type), required when M > 0;
+ *                   values in [0,batch), checked on the device
+ *   shared_input    [shared_rows,N] bfloat16, required when shared_rows > 0
  *   bias            [E,N] bfloat16 (aclnn V3 biasOptional, BF16 on the MX path), or NULL;
  *                   read as a per-expert, per-column term added to the matmul result
  *                   before the logit weighting: out[r,n] += logit * (mm(t,n) + bias[e,n])
  *   out             [batch,N] float32, read and accumulated into in place
- *   prepared        output of gmmfr_prepare_weights for the same x2/scale, or NULL
+ *   prepared        output of gmmfr_prepare_weights for the same x2/scale (prepared_bytes of
+ *                   it, at least gmmfr_prepared_weights_size), or NULL
  *   workspace       at least gmmfr_workspace_size bytes, 256-byte aligned; its
  *                   contents on entry do not matter; it must not be shared by two
  *                   calls in flight at the same time
@@ -177,13 +231,15 @@ GMMFR_API gmmfr_status gmmfr_workspace_size(const gmmfr_problem* problem, int ha
  * Kernels per call: the grouped GEMM alone in the default mode; with
  * GMMFR_DETERMINISTIC the GEMM (which also builds the row CSR of the tokens) and then
  * the combine, a programmatic dependent of the GEMM.  Weights prepared inside the call
- * add the preparation kernel first, and an expanded E2M1 x1 the expansion kernel.
+ * add the preparation kernel first, and an expanded E2M1 x1 the expansion kernel (or,
+ * when K % 16 != 0, the copy of x1 to a 16-byte pitch, which also expands E2M1 codes).
  */
 GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing(
-    const gmmfr_problem* problem, const void* x1, const void* x2, const void* scale,
-    const void* pertoken_scale, const int64_t* group_list, const float* logit,
-    const void* row_index, const void* shared_input, const void* bias, float* out, const void* prepared,
-    void* workspace, size_t workspace_bytes, void* stream);
+    const gmmfr_problem* problem, const gmmfr_tensor* x1, const gmmfr_tensor* x2, const gmmfr_tensor* scale,
+    const gmmfr_tensor* pertoken_scale, const gmmfr_tensor* group_list, const gmmfr_tensor* logit,
+    const gmmfr_tensor* row_index, const gmmfr_tensor* shared_input, const gmmfr_tensor* bias,
+    const gmmfr_tensor* out, const void* prepared, size_t prepared_bytes, void* workspace, size_t workspace_bytes,
+    void* stream);
 
 /*
  * SYNCHRONISES `stream`, then reads the device error word that the last call
@@ -206,7 +262,8 @@ GMMFR_API gmmfr_status gmmfr_check_device_errors(const void* workspace, void* st
  * those 16 MiB until the process exits.  It calls no cudaMalloc / cudaFree.
  *
  *   prepared   required: weights from gmmfr_prepare_weights (the call cannot prepare
- *              them itself); other arguments as for the operator.
+ *              them itself), prepared_bytes of them; other arguments as for the operator
+ *              (views, checked the same way).
  * Problems whose workspace (gmmfr_workspace_size with have_prepared = 1) exceeds
  * 16 MiB are rejected with GMMFR_ERR_WORKSPACE and a message giving both sizes.
  * Outside stream capture each call looks up the array's device address on the current
@@ -220,8 +277,9 @@ GMMFR_API gmmfr_status gmmfr_check_device_errors(const void* workspace, void* st
  * serialised by the caller.
  */
 GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing_static_scratch(
-    const gmmfr_problem* problem, const void* x1, const void* pertoken_scale, const int64_t* group_list,
-    const float* logit, const void* row_index, const void* shared_input, float* out, const void* prepared,
+    const gmmfr_problem* problem, const gmmfr_tensor* x1, const gmmfr_tensor* pertoken_scale,
+    const gmmfr_tensor* group_list, const gmmfr_tensor* logit, const gmmfr_tensor* row_index,
+    const gmmfr_tensor* shared_input, const gmmfr_tensor* out, const void* prepared, size_t prepared_bytes,
     void* stream);
 
 /*

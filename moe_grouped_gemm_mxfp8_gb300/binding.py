@@ -37,6 +37,35 @@ ENTRY_POINTS = (
 DEV_BAD_EXPERT_ID = 8
 
 
+DT_U8, DT_E4M3, DT_E5M2, DT_E2M1X2, DT_E8M0, DT_I64, DT_I32, DT_F32, DT_BF16 = range(9)
+MAX_DIMS = 4
+
+
+class Tensor(ctypes.Structure):
+    """Mirror of gmmfr_tensor: a non-owning view of dense device memory."""
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * MAX_DIMS), ("strides", ctypes.c_int64 * MAX_DIMS)]
+
+
+def raw_view(data, dtype: int, shape, strides=None) -> Tensor:
+    """A view of `data` (an address, or None) with the given dtype code, shape and strides
+    (dense row-major when not given)."""
+    shape = tuple(int(x) for x in shape)
+    if strides is None:
+        strides, acc = [], 1
+        for d in reversed(shape):
+            strides.insert(0, acc)
+            acc *= d
+    t = Tensor()
+    t.data = data
+    t.dtype = dtype
+    t.ndim = len(shape)
+    for i, (d, st) in enumerate(zip(shape, strides)):
+        t.shape[i] = d
+        t.strides[i] = int(st)
+    return t
+
+
 class Problem(ctypes.Structure):
     """Mirror of gmmfr_problem."""
     _fields_ = [
@@ -85,10 +114,11 @@ def load(path: str = LIB_PATH):
             P = ctypes.POINTER(Problem)
             vp, sz = ctypes.c_void_p, ctypes.c_size_t
             lib.gmmfr_prepared_weights_size.argtypes = [P, ctypes.POINTER(sz)]
-            lib.gmmfr_prepare_weights.argtypes = [P, vp, vp, vp, sz, vp]
+            T = ctypes.POINTER(Tensor)
+            lib.gmmfr_prepare_weights.argtypes = [P, T, T, vp, sz, vp]
             lib.gmmfr_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
-            lib.gmmfr_grouped_matmul_finalize_routing.argtypes = [P] + [vp] * 12 + [sz, vp]
-            lib.gmmfr_grouped_matmul_finalize_routing_static_scratch.argtypes = [P] + [vp] * 9
+            lib.gmmfr_grouped_matmul_finalize_routing.argtypes = [P] + [T] * 10 + [vp, sz, vp, sz, vp]
+            lib.gmmfr_grouped_matmul_finalize_routing_static_scratch.argtypes = [P] + [T] * 7 + [vp, sz, vp]
             lib.gmmfr_static_scratch_check_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
             RP = ctypes.POINTER(RouteProblem)
             lib.gmmfr_moe_route_workspace_size.argtypes = [RP, ctypes.POINTER(sz)]
@@ -147,9 +177,14 @@ def gmmfr_prepared_weights_size(problem: Problem) -> int:
     return n.value
 
 
-def gmmfr_prepare_weights(problem: Problem, x2: Optional[int], scale: Optional[int], prepared: Optional[int],
+def _ref(view: Optional[Tensor]):
+    return None if view is None else ctypes.byref(view)
+
+
+def gmmfr_prepare_weights(problem: Problem, x2: Optional[Tensor], scale: Optional[Tensor], prepared: Optional[int],
                           prepared_bytes: int, stream: Optional[int] = None) -> None:
-    _check(load().gmmfr_prepare_weights(ctypes.byref(problem), x2, scale, prepared, prepared_bytes, stream))
+    _check(load().gmmfr_prepare_weights(ctypes.byref(problem), _ref(x2), _ref(scale), prepared, prepared_bytes,
+                                        stream))
 
 
 def gmmfr_workspace_size(problem: Problem, have_prepared: bool) -> int:
@@ -159,21 +194,23 @@ def gmmfr_workspace_size(problem: Problem, have_prepared: bool) -> int:
 
 
 def gmmfr_grouped_matmul_finalize_routing(problem: Problem, x1, x2, scale, pertoken_scale, group_list, logit,
-                                          row_index, shared_input, bias, out, prepared, workspace, workspace_bytes,
-                                          stream=None) -> None:
+                                          row_index, shared_input, bias, out, prepared, prepared_bytes, workspace,
+                                          workspace_bytes, stream=None) -> None:
+    """Tensor arguments are Tensor views (or None); prepared and workspace are addresses."""
     _check(load().gmmfr_grouped_matmul_finalize_routing(
-        ctypes.byref(problem), x1, x2, scale, pertoken_scale, group_list, logit, row_index, shared_input,
-        bias, out, prepared, workspace, workspace_bytes, stream))
+        ctypes.byref(problem), _ref(x1), _ref(x2), _ref(scale), _ref(pertoken_scale), _ref(group_list), _ref(logit),
+        _ref(row_index), _ref(shared_input), _ref(bias), _ref(out), prepared, prepared_bytes, workspace,
+        workspace_bytes, stream))
 
 
 def gmmfr_grouped_matmul_finalize_routing_static_scratch(problem: Problem, x1, pertoken_scale, group_list, logit,
-                                                         row_index, shared_input, out, prepared,
+                                                         row_index, shared_input, out, prepared, prepared_bytes,
                                                          stream=None) -> None:
     """The operator with the library's own 16 MiB device scratch instead of a
     caller workspace (for callers that cannot allocate); needs prepared weights."""
     _check(load().gmmfr_grouped_matmul_finalize_routing_static_scratch(
-        ctypes.byref(problem), x1, pertoken_scale, group_list, logit, row_index, shared_input, out, prepared,
-        stream))
+        ctypes.byref(problem), _ref(x1), _ref(pertoken_scale), _ref(group_list), _ref(logit), _ref(row_index),
+        _ref(shared_input), _ref(out), prepared, prepared_bytes, stream))
 
 
 def gmmfr_static_scratch_check_device_errors(stream=None) -> int:
@@ -252,6 +289,28 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr()
 
 
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.uint8: DT_U8, torch.int64: DT_I64, torch.int32: DT_I32, torch.float32: DT_F32,
+             torch.bfloat16: DT_BF16, torch.float8_e4m3fn: DT_E4M3, torch.float8_e5m2: DT_E5M2}
+    for name, code in (("float8_e8m0fnu", DT_E8M0), ("float4_e2m1fn_x2", DT_E2M1X2)):
+        if hasattr(torch, name):
+            codes[getattr(torch, name)] = code
+    if t.dtype not in codes:
+        raise ValueError(f"gmmfr has no element type for {t.dtype}")
+    return codes[t.dtype]
+
+
+def view(t) -> Optional[Tensor]:
+    """The gmmfr_tensor view of a device tensor (None for None).  The library checks its
+    element type, rank, shape and layout against the problem."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("gmmfr takes device tensors")
+    return raw_view(t.data_ptr(), _dtype_code(t), tuple(t.shape), tuple(t.stride()))
+
+
 def _stream(stream) -> Optional[int]:
     import torch
     if stream is None:
@@ -264,7 +323,7 @@ def prepare_weights(problem: Problem, x2, scale, stream=None):
     import torch
     n = gmmfr_prepared_weights_size(problem)
     buf = torch.empty(max(n, 16), dtype=torch.uint8, device=x2.device)
-    gmmfr_prepare_weights(problem, _ptr(x2), _ptr(scale), _ptr(buf), n, _stream(stream))
+    gmmfr_prepare_weights(problem, view(x2), view(scale), _ptr(buf), n, _stream(stream))
     return buf
 
 
@@ -280,12 +339,20 @@ def run(problem: Problem, inputs: dict, out, prepared=None, ws=None, stream=None
     if ws is None:
         ws = workspace(problem, prepared is not None, out.device)
     gmmfr_grouped_matmul_finalize_routing(
-        problem, _ptr(inputs["x1"]), _ptr(inputs["x2"]) if prepared is None else None,
-        _ptr(inputs["scale"]) if prepared is None else None, _ptr(inputs["pertoken_scale"]),
-        _ptr(inputs["group_list"]), _ptr(inputs.get("logit")), _ptr(inputs["row_index"]),
-        _ptr(inputs.get("shared_input")), _ptr(inputs.get("bias")), _ptr(out), _ptr(prepared), _ptr(ws),
-        ws.numel(), _stream(stream))
+        problem, view(inputs["x1"]), view(inputs["x2"]) if prepared is None else None,
+        view(inputs["scale"]) if prepared is None else None, view(inputs["pertoken_scale"]),
+        view(inputs["group_list"]), view(inputs.get("logit")), view(inputs["row_index"]),
+        view(inputs.get("shared_input")), view(inputs.get("bias")), view(out), _ptr(prepared),
+        0 if prepared is None else prepared.numel(), _ptr(ws), ws.numel(), _stream(stream))
     return ws
+
+
+def run_static_scratch(problem: Problem, inputs: dict, out, prepared, stream=None) -> None:
+    """One call of the allocation-free entry point on device tensors."""
+    gmmfr_grouped_matmul_finalize_routing_static_scratch(
+        problem, view(inputs["x1"]), view(inputs["pertoken_scale"]), view(inputs["group_list"]),
+        view(inputs.get("logit")), view(inputs["row_index"]), view(inputs.get("shared_input")), view(out),
+        _ptr(prepared), prepared.numel(), _stream(stream))
 
 
 def route(topk_ids, topk_weights, x, x_scale, E: int, group_list_type: int = 1, stream=None, ws=None):

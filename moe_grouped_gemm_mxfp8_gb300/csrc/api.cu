@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <initializer_list>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -61,7 +62,8 @@ gmmfr_status validate(const gmmfr_problem* p) {
     return fail(GMMFR_ERR_INVALID_ARG, "expected_tokens_per_expert=%lld is negative", (long long)p->expected_tokens_per_expert);
   if (p->x2_format == GMMFR_E2M1 && !p->transpose_x2 && p->N % 2 != 0)
     return fail(GMMFR_ERR_INVALID_ARG, "N=%lld: an E2M1 x2 that is not transposed needs an even N", (long long)p->N);
-  if (p->K % 16 != 0) return fail(GMMFR_ERR_UNSUPPORTED, "K=%lld: K %% 16 == 0 is required (x1 rows are moved by TMA)", (long long)p->K);
+  if (p->K % 2 != 0 && (p->x1_format == GMMFR_E2M1 || (p->x2_format == GMMFR_E2M1 && p->transpose_x2)))
+    return fail(GMMFR_ERR_INVALID_ARG, "K=%lld: E2M1 codes packed along K need an even K", (long long)p->K);
   return GMMFR_OK;
 }
 
@@ -72,6 +74,11 @@ bool native_fp4(const gmmfr_problem* p) {
   return p->x1_format == GMMFR_E2M1 && p->x2_format == GMMFR_E2M1 && p->K % 32 == 0;
 }
 int64_t k_blocks(const gmmfr_problem* p) { return cdiv(p->K, native_fp4(p) ? gmmfr::kTileK4 : gmmfr::kTileK); }
+// x1 rows the GEMM's TMA cannot read in place: a pitch of K bytes that is not a multiple of 16
+// (they are copied to a 16-byte pitch), or E2M1 codes that are expanded to E4M3 first.
+bool pad_tokens(const gmmfr_problem* p) { return !native_fp4(p) && p->K % 16 != 0; }
+bool expand_tokens(const gmmfr_problem* p) { return p->x1_format == GMMFR_E2M1 && !native_fp4(p); }
+int64_t token_pitch(const gmmfr_problem* p) { return pad_tokens(p) ? cdiv(p->K, 16) * 16 : p->K; }
 size_t prepared_bytes(const gmmfr_problem* p) {
   return (size_t)p->E * cdiv(p->N, gmmfr::kTileN) * k_blocks(p) *
          (native_fp4(p) ? gmmfr::kPrepTileBytes4 : gmmfr::kPrepTileBytes);
@@ -144,9 +151,9 @@ Layout make_layout(const gmmfr_problem* p, bool have_prepared) {
     L.off_prep = off;
     off = align256(off + prepared_bytes(p));
   }
-  if (p->x1_format == GMMFR_E2M1 && !native_fp4(p)) {  // E2M1 tokens expanded to E4M3 codes, [M, K] bytes
+  if (expand_tokens(p) || pad_tokens(p)) {  // tokens as E4M3 / FP8 codes at a 16-byte pitch, [M, Kp] bytes
     L.off_tok = off;
-    off = align256(off + (size_t)p->M * p->K);
+    off = align256(off + (size_t)p->M * token_pitch(p));
   }
   L.total = off;
   return L;
@@ -193,6 +200,61 @@ struct CallTimer {
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
 
+// ---------------------------------------------------------------- tensor views
+const char* dtype_name(int32_t dt) {
+  static const char* names[] = {"U8", "E4M3", "E5M2", "E2M1X2", "E8M0", "I64", "I32", "F32", "BF16"};
+  return dt >= 0 && dt <= GMMFR_DT_BF16 ? names[dt] : "unknown";
+}
+
+std::string dims_text(const int64_t* d, int n) {
+  std::string t = "[";
+  for (int i = 0; i < n; ++i) t += (i ? "," : "") + std::to_string(d[i]);
+  return t + "]";
+}
+
+// An FP operand's element type: raw bytes, or the typed code of its format.
+bool operand_dtype_ok(int32_t dt, int32_t fmt) {
+  return dt == GMMFR_DT_U8 || (fmt == GMMFR_E4M3 && dt == GMMFR_DT_E4M3) ||
+         (fmt == GMMFR_E5M2 && dt == GMMFR_DT_E5M2) || (fmt == GMMFR_E2M1 && dt == GMMFR_DT_E2M1X2);
+}
+bool scale_dtype_ok(int32_t dt) { return dt == GMMFR_DT_U8 || dt == GMMFR_DT_E8M0; }
+
+// A view present or not: `required` views may be absent only when the call computes nothing.
+// Checks the element type, the rank and shape against `shape`, a dense row-major layout, and
+// a non-NULL address when the tensor has elements.
+gmmfr_status check_view(const gmmfr_tensor* t, const char* name, bool required, bool dtype_ok, const char* want_dtype,
+                        std::initializer_list<int64_t> shape) {
+  const int n = (int)shape.size();
+  if (!t) return required ? fail(GMMFR_ERR_INVALID_ARG, "%s is required (NULL view)", name) : GMMFR_OK;
+  if (!dtype_ok)
+    return fail(GMMFR_ERR_INVALID_ARG, "%s: element type %s (%d), expected %s", name, dtype_name(t->dtype), t->dtype,
+                want_dtype);
+  if (t->ndim < 1 || t->ndim > GMMFR_MAX_DIMS)
+    return fail(GMMFR_ERR_INVALID_ARG, "%s: rank %d out of range [1, 4]", name, t->ndim);
+  int64_t want[GMMFR_MAX_DIMS];
+  int i = 0;
+  for (int64_t v : shape) want[i++] = v;
+  if (t->ndim != n)
+    return fail(GMMFR_ERR_INVALID_ARG, "%s: rank %d, expected %d (shape %s)", name, t->ndim, n,
+                dims_text(want, n).c_str());
+  for (i = 0; i < n; ++i)
+    if (t->shape[i] != want[i])
+      return fail(GMMFR_ERR_INVALID_ARG, "%s: shape %s does not match the problem's %s", name,
+                  dims_text(t->shape, n).c_str(), dims_text(want, n).c_str());
+  int64_t dense = 1, numel = 1;
+  for (i = n - 1; i >= 0; --i) {
+    if (t->shape[i] != 1 && t->strides[i] != dense)
+      return fail(GMMFR_ERR_INVALID_ARG, "%s: strides %s are not the dense row-major strides of shape %s", name,
+                  dims_text(t->strides, n).c_str(), dims_text(t->shape, n).c_str());
+    dense *= t->shape[i];
+    numel *= t->shape[i];
+  }
+  if (numel > 0 && !t->data) return fail(GMMFR_ERR_INVALID_ARG, "%s: data is NULL", name);
+  return GMMFR_OK;
+}
+
+void* view_data(const gmmfr_tensor* t) { return t ? t->data : nullptr; }
+
 }  // namespace
 
 namespace gmmfr {
@@ -236,13 +298,40 @@ static gmmfr::PrepParams prep_params(const gmmfr_problem* p, const void* x2, con
   return pp;
 }
 
-gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const void* x2, const void* scale, void* prepared,
-                                   size_t prepared_bytes, void* stream) {
+static const char* operand_dtype_text(int32_t fmt) {
+  return fmt == GMMFR_E4M3 ? "E4M3 or U8" : (fmt == GMMFR_E5M2 ? "E5M2 or U8" : "E2M1X2 or U8");
+}
+
+// The raw weights' views: x2 [E,K,N] or [E,N,K] (E2M1: the packed last dimension halved) and
+// scale [(E,)ceil(K/64),N,2] or [(E,)N,ceil(K/64),2] (section 3.1 tensor table; aclnn V3's
+// 4-D per-expert form).
+static gmmfr_status check_weight_views(const gmmfr_problem& p, const gmmfr_tensor* x2, const gmmfr_tensor* scale,
+                                       bool required) {
+  const int64_t Ks = cdiv(p.K, 64);
+  const bool e2 = p.x2_format == GMMFR_E2M1;
+  const bool x2_ok = x2 && operand_dtype_ok(x2->dtype, p.x2_format);
+  const char* x2_dt = operand_dtype_text(p.x2_format);
+  gmmfr_status st = p.transpose_x2 ? check_view(x2, "x2", required, x2_ok, x2_dt, {p.E, p.N, e2 ? p.K / 2 : p.K})
+                                   : check_view(x2, "x2", required, x2_ok, x2_dt, {p.E, p.K, e2 ? p.N / 2 : p.N});
+  if (st) return st;
+  const bool sc_ok = scale && scale_dtype_ok(scale->dtype);
+  if (p.scale_per_expert)
+    return p.transpose_x2 ? check_view(scale, "scale", required, sc_ok, "E8M0 or U8", {p.E, p.N, Ks, 2})
+                          : check_view(scale, "scale", required, sc_ok, "E8M0 or U8", {p.E, Ks, p.N, 2});
+  return p.transpose_x2 ? check_view(scale, "scale", required, sc_ok, "E8M0 or U8", {p.N, Ks, 2})
+                        : check_view(scale, "scale", required, sc_ok, "E8M0 or U8", {Ks, p.N, 2});
+}
+
+gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const gmmfr_tensor* x2_view,
+                                   const gmmfr_tensor* scale_view, void* prepared, size_t prepared_bytes,
+                                   void* stream) {
   if (gmmfr_status st = validate(problem)) return st;
   size_t need = 0;
   gmmfr_prepared_weights_size(problem, &need);
   if (problem->N == 0) return GMMFR_OK;
-  if (!x2 || !scale) return fail(GMMFR_ERR_INVALID_ARG, "x2 and scale must be non-NULL");
+  if (gmmfr_status st = check_weight_views(*problem, x2_view, scale_view, true)) return st;
+  const void* x2 = view_data(x2_view);
+  const void* scale = view_data(scale_view);
   if (!prepared) return fail(GMMFR_ERR_INVALID_ARG, "prepared is NULL");
   if (prepared_bytes < need) return fail(GMMFR_ERR_WORKSPACE, "prepared buffer has %zu bytes, needs %zu", prepared_bytes, need);
   if (!aligned(prepared, 16)) return fail(GMMFR_ERR_WORKSPACE, "prepared buffer must be 16-byte aligned");
@@ -251,14 +340,13 @@ gmmfr_status gmmfr_prepare_weights(const gmmfr_problem* problem, const void* x2,
   return GMMFR_OK;
 }
 
-gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem, const void* x1, const void* x2,
-                                                   const void* scale, const void* pertoken_scale,
-                                                   const int64_t* group_list, const float* logit,
-                                                   const void* row_index, const void* shared_input,
-                                                   const void* bias, float* out,
-                                                   const void* prepared, void* workspace, size_t workspace_bytes,
-                                                   void* stream) {
-  if (gmmfr_status st = validate(problem)) return st;
+}  // extern "C"
+
+// The operator on plain device pointers, once its views have been checked.
+static gmmfr_status operator_call(const gmmfr_problem* problem, const void* x1, const void* x2, const void* scale,
+                                  const void* pertoken_scale, const int64_t* group_list, const float* logit,
+                                  const void* row_index, const void* shared_input, const void* bias, float* out,
+                                  const void* prepared, void* workspace, size_t workspace_bytes, void* stream) {
   const gmmfr_problem& p = *problem;
   const bool det = p.flags & GMMFR_DETERMINISTIC;
   if (p.N == 0 || p.batch == 0 && p.M == 0) return GMMFR_OK;  // nothing to compute
@@ -268,7 +356,8 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   if (p.batch > 0 && !out) return fail(GMMFR_ERR_INVALID_ARG, "out is NULL");
   if (p.shared_rows > 0 && !shared_input) return fail(GMMFR_ERR_INVALID_ARG, "shared_input is NULL but shared_rows > 0");
   if (!prepared && (!x2 || !scale)) return fail(GMMFR_ERR_INVALID_ARG, "either prepared or both x2 and scale must be given");
-  if (x1 && !aligned(x1, 16)) return fail(GMMFR_ERR_INVALID_ARG, "x1 must be 16-byte aligned");
+  if (x1 && !expand_tokens(problem) && !pad_tokens(problem) && !aligned(x1, 16))
+    return fail(GMMFR_ERR_INVALID_ARG, "x1 must be 16-byte aligned");
   if (prepared && !aligned(prepared, 16)) return fail(GMMFR_ERR_INVALID_ARG, "prepared must be 16-byte aligned");
   if (!aligned(group_list, 8) || (row_index && !aligned(row_index, p.row_index_type == GMMFR_INDEX_I32 ? 4 : 8)) ||
       (logit && !aligned(logit, 4)) || (out && !aligned(out, 4)) || (shared_input && !aligned(shared_input, 2)) ||
@@ -291,26 +380,32 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   const uint8_t* wprep = static_cast<const uint8_t*>(prepared);
   timer.begin(4, s);
   const bool fp4 = native_fp4(problem);
-  const bool fp4_tokens = p.x1_format == GMMFR_E2M1 && !fp4 && p.M > 0;
-  if (!prepared || fp4_tokens) timer.begin(0, s);
+  const bool fp4_tokens = expand_tokens(problem) && p.M > 0;
+  const bool padded_tokens = pad_tokens(problem) && p.M > 0;
+  if (!prepared || fp4_tokens || padded_tokens) timer.begin(0, s);
   if (!prepared) {
     e = gmmfr::launch_prep(prep_params(problem, x2, scale, ws + L.off_prep), s);
     if (e != cudaSuccess) return cuda_fail(e, "weight preparation launch");
     wprep = ws + L.off_prep;
   }
-  if (fp4_tokens) {  // tokens: E2M1 -> E4M3, exact
+  if (padded_tokens) {  // tokens at a 16-byte pitch (E2M1 expanded to E4M3 on the way, exact)
+    e = gmmfr::launch_pad_tokens(static_cast<const uint8_t*>(x1), ws + L.off_tok, p.M, p.K, token_pitch(problem),
+                                 p.x1_format == GMMFR_E2M1, s);
+    if (e != cudaSuccess) return cuda_fail(e, "token copy launch");
+    x1 = ws + L.off_tok;
+  } else if (fp4_tokens) {  // tokens: E2M1 -> E4M3, exact
     e = gmmfr::launch_expand_fp4(static_cast<const uint8_t*>(x1), ws + L.off_tok, p.M * p.K / 2, s);
     if (e != cudaSuccess) return cuda_fail(e, "token FP4 expansion launch");
     x1 = ws + L.off_tok;
   }
-  if (!prepared || fp4_tokens) timer.end(0, s);
+  if (!prepared || fp4_tokens || padded_tokens) timer.end(0, s);
 
   // x1 [M, K] bytes (packed E2M1: [M, K/2]) as 2-D tensors of 128-byte rows: boxes of 16, 32,
   // 64, 128 rows, 128-byte swizzle
   gmmfr::TokenMaps tmaps;
   {
     const bool empty = p.M == 0;
-    const int64_t row_bytes = fp4 ? p.K / 2 : p.K;
+    const int64_t row_bytes = fp4 ? p.K / 2 : token_pitch(problem);
     cuuint64_t dims[2] = {(cuuint64_t)(empty ? 16 : row_bytes), (cuuint64_t)(empty ? 1 : p.M)};
     cuuint64_t strides[1] = {(cuuint64_t)(empty ? 16 : row_bytes)};
     cuuint32_t estr[2] = {1, 1};
@@ -403,6 +498,54 @@ gmmfr_status gmmfr_grouped_matmul_finalize_routing(const gmmfr_problem* problem,
   }
   timer.end(4, s);
   return GMMFR_OK;
+}
+
+extern "C" {
+
+gmmfr_status gmmfr_grouped_matmul_finalize_routing(
+    const gmmfr_problem* problem, const gmmfr_tensor* x1, const gmmfr_tensor* x2, const gmmfr_tensor* scale,
+    const gmmfr_tensor* pertoken_scale, const gmmfr_tensor* group_list, const gmmfr_tensor* logit,
+    const gmmfr_tensor* row_index, const gmmfr_tensor* shared_input, const gmmfr_tensor* bias, const gmmfr_tensor* out,
+    const void* prepared, size_t prepared_bytes, void* workspace, size_t workspace_bytes, void* stream) {
+  if (gmmfr_status st = validate(problem)) return st;
+  const gmmfr_problem& p = *problem;
+  // a call with nothing to compute (N == 0, or no rows and no tokens) needs no tensor; the
+  // views that are given are checked all the same
+  const bool work = !(p.N == 0 || (p.batch == 0 && p.M == 0));
+  const int64_t Ks = cdiv(p.K, 64);
+  const bool e1 = p.x1_format == GMMFR_E2M1;
+  gmmfr_status st;
+  if ((st = check_view(x1, "x1", work && p.M > 0, x1 && operand_dtype_ok(x1->dtype, p.x1_format),
+                       operand_dtype_text(p.x1_format), {p.M, e1 ? p.K / 2 : p.K})))
+    return st;
+  if ((st = check_weight_views(p, x2, scale, work && !prepared))) return st;
+  if ((st = check_view(pertoken_scale, "pertoken_scale", work && p.M > 0,
+                       pertoken_scale && scale_dtype_ok(pertoken_scale->dtype), "E8M0 or U8", {p.M, Ks, 2})))
+    return st;
+  if ((st = check_view(group_list, "group_list", work, group_list && group_list->dtype == GMMFR_DT_I64, "I64", {p.E})))
+    return st;
+  if ((st = check_view(logit, "logit", false, logit && logit->dtype == GMMFR_DT_F32, "F32", {p.M}))) return st;
+  const int32_t row_dt = p.row_index_type == GMMFR_INDEX_I32 ? GMMFR_DT_I32 : GMMFR_DT_I64;
+  if ((st = check_view(row_index, "row_index", work && p.M > 0, row_index && row_index->dtype == row_dt,
+                       row_dt == GMMFR_DT_I32 ? "I32 (row_index_type)" : "I64 (row_index_type)", {p.M})))
+    return st;
+  if ((st = check_view(shared_input, "shared_input", work && p.shared_rows > 0,
+                       shared_input && shared_input->dtype == GMMFR_DT_BF16, "BF16", {p.shared_rows, p.N})))
+    return st;
+  if ((st = check_view(bias, "bias", false, bias && bias->dtype == GMMFR_DT_BF16, "BF16", {p.E, p.N}))) return st;
+  if ((st = check_view(out, "out", work && p.batch > 0, out && out->dtype == GMMFR_DT_F32, "F32", {p.batch, p.N})))
+    return st;
+  if (prepared) {
+    size_t need = 0;
+    gmmfr_prepared_weights_size(problem, &need);
+    if (prepared_bytes < need)
+      return fail(GMMFR_ERR_WORKSPACE, "prepared buffer has %zu bytes, needs %zu", prepared_bytes, need);
+  }
+  if (!work) return GMMFR_OK;
+  return operator_call(problem, view_data(x1), view_data(x2), view_data(scale), view_data(pertoken_scale),
+                       static_cast<const int64_t*>(view_data(group_list)), static_cast<const float*>(view_data(logit)),
+                       view_data(row_index), view_data(shared_input), view_data(bias),
+                       static_cast<float*>(view_data(out)), prepared, workspace, workspace_bytes, stream);
 }
 
 static gmmfr_status validate_route(const gmmfr_route_problem* p) {

@@ -46,6 +46,9 @@ struct PrepParams {
   int32_t fp4_native;  // with fp4: keep them packed (256-K tiles for kind::mxf4), else expand to E4M3
 };
 cudaError_t launch_expand_fp4(const uint8_t* packed, uint8_t* fp8, int64_t n_bytes, cudaStream_t s);
+// x1 [M, K] (packed E2M1 with fp4) -> [M, Kp] bytes, Kp = K rounded up to 16, zero past K
+cudaError_t launch_pad_tokens(const uint8_t* x1, uint8_t* dst, int64_t M, int64_t K, int64_t Kp, bool fp4,
+                              cudaStream_t s);
 
 struct GemmParams {
   const uint8_t* prepared;

@@ -1,5 +1,6 @@
 // Auxiliary kernels of MXFP8 grouped-matmul-finalize-routing:
-//   - E2M1 (MXFP4) token expansion to E4M3,
+//   - E2M1 (MXFP4) token expansion to E4M3, and the copy of x1 rows to a 16-byte pitch
+//     (K % 16 != 0),
 //   - weight preparation (one-time re-layout of x2 and its scales into GEMM tiles),
 //   - deterministic combine (row-ordered sum of the per-token results; the row CSR
 //     of the routed tokens it walks is built inside the grouped GEMM kernel).
@@ -75,6 +76,40 @@ cudaError_t launch_expand_fp4(const uint8_t* packed, uint8_t* fp8, int64_t n_byt
   const int64_t work = vec ? n_vec / 16 + (n_bytes - n_vec) : n_bytes;
   const int64_t blocks = (work + 255) / 256;
   expand_fp4_kernel<<<(unsigned)(blocks < sms * 4 ? blocks : sms * 4), 256, 0, s>>>(packed, fp8, n_bytes, n_vec);
+  return cudaGetLastError();
+}
+
+// x1 rows re-laid at a pitch of Kp = K rounded up to 16 bytes (TMA moves rows whose pitch is a
+// multiple of 16 bytes): dst[t, k] = x1[t, k] for k < K and 0 for K <= k < Kp.  With `fp4` the
+// source rows hold packed E2M1 codes (K/2 bytes, K even) and are expanded to E4M3 on the way.
+// Zero codes past K meet zero weight bytes in the prepared tiles, so they add nothing.
+__global__ void __launch_bounds__(256) pad_tokens_kernel(const uint8_t* src, uint8_t* dst, int64_t M, int64_t K,
+                                                         int64_t Kp, int32_t fp4) {
+  const int64_t n = M * Kp;
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    const int64_t t = i / Kp, k = i - t * Kp;
+    uint8_t v = 0;
+    if (k < K) {
+      if (fp4) {
+        const uint32_t b = src[t * (K / 2) + k / 2];
+        v = e2m1_to_e4m3((k & 1) ? b >> 4 : b & 15);
+      } else {
+        v = src[t * K + k];
+      }
+    }
+    dst[i] = v;
+  }
+}
+
+cudaError_t launch_pad_tokens(const uint8_t* x1, uint8_t* dst, int64_t M, int64_t K, int64_t Kp, bool fp4,
+                              cudaStream_t s) {
+  const int64_t n = M * Kp;
+  if (n == 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t blocks = (n + 255) / 256;
+  pad_tokens_kernel<<<(unsigned)(blocks < sms * 8 ? blocks : sms * 8), 256, 0, s>>>(x1, dst, M, K, Kp, fp4 ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -59,8 +59,9 @@ gmmfr_status scratch_address(cudaStream_t stream, void** out) {
 }  // namespace
 
 extern "C" GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing_static_scratch(
-    const gmmfr_problem* problem, const void* x1, const void* pertoken_scale, const int64_t* group_list,
-    const float* logit, const void* row_index, const void* shared_input, float* out, const void* prepared,
+    const gmmfr_problem* problem, const gmmfr_tensor* x1, const gmmfr_tensor* pertoken_scale,
+    const gmmfr_tensor* group_list, const gmmfr_tensor* logit, const gmmfr_tensor* row_index,
+    const gmmfr_tensor* shared_input, const gmmfr_tensor* out, const void* prepared, size_t prepared_bytes,
     void* stream) {
   size_t need = 0;
   if (gmmfr_status st = gmmfr_workspace_size(problem, 1, &need)) return st;
@@ -78,8 +79,8 @@ extern "C" GMMFR_API gmmfr_status gmmfr_grouped_matmul_finalize_routing_static_s
   // The operator overwrites every scratch word it reads (header, group table,
   // token scales, CSR) before reading it, so nothing has to be cleared here.
   return gmmfr_grouped_matmul_finalize_routing(problem, x1, nullptr, nullptr, pertoken_scale, group_list, logit,
-                                               row_index, shared_input, nullptr, out, prepared, scratch,
-                                               kStaticScratchBytes, stream);
+                                               row_index, shared_input, nullptr, out, prepared, prepared_bytes,
+                                               scratch, kStaticScratchBytes, stream);
 }
 
 extern "C" GMMFR_API gmmfr_status gmmfr_static_scratch_check_device_errors(void* stream, uint32_t* bits) {

@@ -148,6 +148,19 @@ SMALL = {
     "e4m3_tokens_mxfp4_weights": dict(x2_dtype=W.E2M1, transpose_x2=True, scale_per_expert=True, bias=True,
                                       N=255),
     "mxfp4_k16_n2": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, K=16, N=2, M=7, batch=5),  # 56-byte packed x1
+    # K % 16 != 0 (the aclnn V3 constraints and the ceil(K/64) scale layout of section 3.1 admit any
+    # K): x1 rows are copied to a 16-byte pitch first (E2M1 codes expanded on the way)
+    "k40": dict(K=40),
+    "k72_t": dict(K=72, transpose_x2=True, rows="random", out_init="randn"),
+    "k200": dict(K=200, E=3, M=70, counts="explicit", explicit_counts=(33, 0, 37), bias=True),
+    "k200_t_e5m2": dict(K=200, transpose_x2=True, x1_dtype=W.E5M2, x2_dtype=W.E5M2, group_list_type=0,
+                        scale_per_expert=True),
+    "k1": dict(K=1, N=130),
+    "k8_n3": dict(K=8, N=3, M=9, batch=4),
+    "k1032_split": dict(K=1032, E=4, M=60, N=320, rows="random", out_init="randn"),  # K blocks split over CTAs
+    "mxfp4_k40": dict(x1_dtype=W.E2M1, x2_dtype=W.E2M1, K=40, N=64),
+    "mxfp4_tokens_k72_t": dict(x1_dtype=W.E2M1, x2_dtype=W.E4M3, K=72, transpose_x2=True),
+    "mxfp4_weights_k200_t": dict(x2_dtype=W.E2M1, K=200, transpose_x2=True, N=130),
     "mxfp4_straddle": dict(E=9, M=1344, batch=200, N=256, K=128, rows="random", x1_dtype=W.E2M1,
                            x2_dtype=W.E2M1, counts="explicit",
                            explicit_counts=(63, 64, 65, 127, 128, 129, 255, 256, 257)),
@@ -163,7 +176,7 @@ def test_small_atomic(name):
 # scalar path
 @pytest.mark.parametrize("name", ["basic", "transposed", "ragged_counts", "random_rows_shared", "straddle", "k96",
                                   "bias_split_k", "mxfp4_t", "mxfp4_k352_bias", "k16_n1", "mxfp4_k96",
-                                  "e4m3_tokens_mxfp4_weights"])
+                                  "e4m3_tokens_mxfp4_weights", "k72_t", "k1032_split", "mxfp4_k40"])
 def test_small_deterministic(name):
     spec = _spec(**SMALL[name])
     inp = W.make_inputs(spec)

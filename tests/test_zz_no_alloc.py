@@ -35,9 +35,8 @@ def _ready():
 
 def _static_call(prob, d, out, prep, stream):
     B.gmmfr_grouped_matmul_finalize_routing_static_scratch(
-        prob, d["x1"].data_ptr(), d["pertoken_scale"].data_ptr(), d["group_list"].data_ptr(),
-        d["logit"].data_ptr(), d["row_index"].data_ptr(), d["shared_input"].data_ptr(), out.data_ptr(),
-        prep.data_ptr(), stream)
+        prob, B.view(d["x1"]), B.view(d["pertoken_scale"]), B.view(d["group_list"]), B.view(d["logit"]),
+        B.view(d["row_index"]), B.view(d["shared_input"]), B.view(out), prep.data_ptr(), prep.numel(), stream)
 
 
 # E2M1 tokens with E4M3 weights: the tokens are expanded to E4M3 inside the call, into the
@@ -103,9 +102,11 @@ def test_static_scratch_refuses_oversized_problems():
     big = B.make_problem(M=4096, K=7168, N=4096, E=256, batch=512, deterministic=True)
     assert B.gmmfr_workspace_size(big, True) > 16 << 20
     with pytest.raises(B.GmmfrError) as ei:
-        B.gmmfr_grouped_matmul_finalize_routing_static_scratch(big, None, None, None, None, None, None, None, 256)
+        B.gmmfr_grouped_matmul_finalize_routing_static_scratch(big, None, None, None, None, None, None, None, 256,
+                                                               1 << 40)
     assert ei.value.status == B.ERR_WORKSPACE and "16 MiB" in str(ei.value)
     small = B.make_problem(M=16, K=128, N=128, E=1, batch=16)
     with pytest.raises(B.GmmfrError) as ei:
-        B.gmmfr_grouped_matmul_finalize_routing_static_scratch(small, None, None, None, None, None, None, None, None)
+        B.gmmfr_grouped_matmul_finalize_routing_static_scratch(small, None, None, None, None, None, None, None, None,
+                                                               0)
     assert ei.value.status == B.ERR_INVALID_ARG and "gmmfr_prepare_weights" in str(ei.value)
