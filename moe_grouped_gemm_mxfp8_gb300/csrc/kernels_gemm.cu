@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      if (p.test_stall) ok = wait_bar(ptx::smem_u32(stall), 0, ctl);
+      if (p.test_stall) ok = wait_bar<!det>(ptx::smem_u32(stall), 0, ctl);
       Seg sg;
       int e = -1;
       while (ok && sched.next<det>(sg)) {
@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
         // sibling groups of the same expert read the same weight tiles shortly after
         const uint64_t pol_w = (s_gbase[e + 1] - s_gbase[e]) > 1 ? pol_keep : pol_stream;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-          if (!wait_bar(ptx::smem_u32(&empty[stage]), phase ^ 1, ctl)) {
+          if (!wait_bar<!det>(ptx::smem_u32(&empty[stage]), phase ^ 1, ctl)) {
             ok = false;
             break;
           }
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       if (ok) {  // all fills consumed: wait until the MMA warp has released every stage
         for (int s = 0; s < n_stages; ++s) {
           const int64_t fs = n_fill / n_stages + (s < n_fill % n_stages ? 1 : 0);
-          if (fs > 0 && !wait_bar(ptx::smem_u32(&empty[s]), (uint32_t)((fs - 1) & 1), ctl)) break;
+          if (fs > 0 && !wait_bar<!det>(ptx::smem_u32(&empty[s]), (uint32_t)((fs - 1) & 1), ctl)) break;
         }
       }
       if (*abort_flag) {  // aborted: let every issued copy land before shared memory is released
@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
         const uint32_t idesc = p.idesc | ((npad >> 3) << 17);
         const int buf = acc_i & 1;
         const uint32_t aph = (acc_i >> 1) & 1;
-        if (!wait_bar(ptx::smem_u32(&acce[buf]), aph ^ 1, ctl)) break;
+        if (!wait_bar<!det>(ptx::smem_u32(&acce[buf]), aph ^ 1, ctl)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * tmax;
         // packed E2M1 is paced by this loop: four stages per iteration cut its fixed cost per
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
         // longer stays in the instruction cache); no gain for FP8, which HBM paces
 #pragma unroll(fp4 ? 4 : 1)
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-          if (!wait_bar(ptx::smem_u32(&full[stage]), phase, ctl)) {
+          if (!wait_bar<!det>(ptx::smem_u32(&full[stage]), phase, ctl)) {
             ok = false;
             break;
           }
@@ -716,7 +716,7 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       int stage = par;  // item n fills stage n % n_stages (n_stages >= 6)
       uint32_t phase = 0;
       while (v0) {
-        if (!warp_wait_bar(ptx::smem_u32(&empty[stage]), phase ^ 1, ctl)) break;
+        if (!warp_wait_bar<!det>(ptx::smem_u32(&empty[stage]), phase ^ 1, ctl)) break;
         uint8_t* xsf = smem + stage * stage_bytes + off_xsf;
 #pragma unroll
         for (int r = 0; r < 4; ++r) *reinterpret_cast<uint32_t*>(xsf + 16 * lane + 4 * r) = w0[r];
@@ -777,36 +777,49 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       }
       ptx::bar_sync(1, 128);
       const uint32_t aph = (acc_i >> 1) & 1;
-      if (!warp_wait_bar(ptx::smem_u32(&accf[buf]), aph, ctl)) break;
+      if (!warp_wait_bar<!det>(ptx::smem_u32(&accf[buf]), aph, ctl)) break;
       ptx::tc_fence_after();
       const int64_t n = (int64_t)sg.j * kTileN + q * 32 + lane;
       const bool n_ok = n < p.N;
       // the bias term is added once per (token, column): by the segment holding K block 0
       const float bias_n = (p.bias != nullptr && sg.kb0 == 0 && n_ok) ? bf16f(p.bias[(int64_t)e * p.N + n]) : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * tmax;
-      for (int c0 = 0; c0 < T; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(taddr + c0, v);
-        ptx::tmem_wait_ld();
-        if (c0 + 32 >= T) {  // accumulator fully read: hand it back to the MMA warp
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acce[buf]));
-        }
-        const int cnt = T - c0 < 32 ? T - c0 : 32;
-        const int32_t* rows = s_trow + buf * 128 + c0;  // read as broadcasts
-        const float* lgs = s_tlg + buf * 128 + c0;
-        // one unrolled loop per mode, so the atomic mode's hot code holds no store path of
-        // the deterministic one (the instruction cache is the scarce resource here)
-        if constexpr (det) {
+      // one loop per mode, so the atomic mode's hot code holds no store path of the
+      // deterministic one (the instruction cache is the scarce resource here)
+      if constexpr (det) {  // 32 tokens per TMEM load, stored into the per-token buffer
+        for (int c0 = 0; c0 < T; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c0, v);
+          ptx::tmem_wait_ld();
+          if (c0 + 32 >= T) {  // accumulator fully read: hand it back to the MMA warp
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acce[buf]));
+          }
+          const int cnt = T - c0 < 32 ? T - c0 : 32;
+          const float* lgs = s_tlg + buf * 128 + c0;  // read as broadcasts
           float* y = p.ybuf + ((int64_t)sg.slot * p.M + t0 + c0) * p.N + n;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj)
             if (jj < cnt && n_ok) y[(int64_t)jj * p.N] = (__uint_as_float(v[jj]) + bias_n) * lgs[jj];
-        } else {
-          float* o = p.out + n;
+        }
+      } else {  // 8 tokens per TMEM load: a quarter of the unrolled scatter code of 32 (C1 37.5 ->
+                // 37.3 us, C2 80.6 -> 79.9, C5 1089.1 -> 1088.4)
+        float* o = p.out + n;
+        for (int c0 = 0; c0 < T; c0 += 8) {
+          uint32_t v[8];
+          ptx::tmem_ld_32x32b_x8(taddr + c0, v);
+          ptx::tmem_wait_ld();
+          if (c0 + 8 >= T) {  // accumulator fully read: hand it back to the MMA warp
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acce[buf]));
+          }
+          const int cnt = T - c0 < 8 ? T - c0 : 8;
+          const int32_t* rows = s_trow + buf * 128 + c0;  // read as broadcasts
+          const float* lgs = s_tlg + buf * 128 + c0;
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
+          for (int jj = 0; jj < 8; ++jj) {
             if (jj < cnt) {
               const int row = rows[jj];
               if (n_ok && row >= 0) ptx::red_add_f32(o + (int64_t)row * p.N, (__uint_as_float(v[jj]) + bias_n) * lgs[jj]);

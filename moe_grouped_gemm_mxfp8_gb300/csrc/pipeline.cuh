@@ -15,10 +15,9 @@ struct Ctl {
   int64_t timeout_ns;
 };
 
-// The polling loop of wait_bar, out of line: every role's stage loop inlines only the first
-// try_wait, which keeps those loops small (the SMs' instruction caches are the scarce resource
-// of the persistent kernels: C1 37.9 -> 37.5 us, C5 1082.4 -> 1081.7 us per call).
-static __device__ __noinline__ bool wait_bar_poll(uint32_t bar, uint32_t parity, Ctl c) {
+// The polling loop of a bounded wait: gives up when another role aborted or after
+// timeout_ns (then records the timeout and aborts).
+__device__ __forceinline__ bool wait_bar_loop(uint32_t bar, uint32_t parity, const Ctl& c) {
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -30,19 +29,28 @@ static __device__ __noinline__ bool wait_bar_poll(uint32_t bar, uint32_t parity,
     }
   }
 }
+static __device__ __noinline__ bool wait_bar_poll(uint32_t bar, uint32_t parity, Ctl c) {
+  return wait_bar_loop(bar, parity, c);
+}
 
-// Bounded wait for the phase of `parity` to complete.  Gives up when another
-// role aborted or after timeout_ns (then records the timeout and aborts).
+// Bounded wait for the phase of `parity` to complete.  kOutOfLine: only the first try_wait is
+// inlined and the polling loop is one shared out-of-line function, which keeps the role loops
+// that call it small (the persistent kernels' instruction caches are their scarce resource:
+// atomic-mode C1 37.9 -> 37.5 us, C5 1082.4 -> 1081.7 us per call); the deterministic
+// instantiations, whose register budget the call disturbs (C5 1150 -> 1156 us), inline it.
+template <bool kOutOfLine = true>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_bar_poll(bar, parity, c);
+  if constexpr (kOutOfLine) return wait_bar_poll(bar, parity, c);
+  else return wait_bar_loop(bar, parity, c);
 }
 
 // wait_bar for a whole warp: every lane waits in hardware (the warp stays
 // converged and sleeps in try_wait), then a vote makes the outcome uniform, so
 // a timeout seen by one lane can never split the warp.
+template <bool kOutOfLine = true>
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
-  const bool ok = wait_bar(bar, parity, c);
+  const bool ok = wait_bar<kOutOfLine>(bar, parity, c);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
