@@ -250,8 +250,9 @@ def _mutant_runs(lib_path, p, rows, cols):
 def test_parity_tolerance_rejects_each_arithmetic_mistake(mutant_libs):
     """The GPU parity tests accept a result within oracle.tolerance of the oracle and with the
     same error flags.  Each planted mistake, if it were the kernel's, would fail that check on
-    at least one small workload of the kinds the GPU suite runs (the full comparison, or the
-    sampled one used at full size)."""
+    at least one small workload of the kinds the GPU suite runs (the GPU suite compares every
+    element; mistakes planted in the oracle's per-element entry point are judged by that entry
+    point's output)."""
     import numpy as np
 
     import oracle
