@@ -785,22 +785,23 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       const float bias_n = (p.bias != nullptr && sg.kb0 == 0 && n_ok) ? bf16f(p.bias[(int64_t)e * p.N + n]) : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * tmax;
       // one loop per mode, so the atomic mode's hot code holds no store path of the
-      // deterministic one (the instruction cache is the scarce resource here)
-      if constexpr (det) {  // 32 tokens per TMEM load, stored into the per-token buffer
-        for (int c0 = 0; c0 < T; c0 += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c0, v);
+      // deterministic one (the instruction cache is the scarce resource here); 8 tokens per TMEM
+      // load in both, a quarter of the unrolled code of 32 (deterministic C5 1150 -> 1147 us)
+      if constexpr (det) {  // stored into the per-token buffer
+        for (int c0 = 0; c0 < T; c0 += 8) {
+          uint32_t v[8];
+          ptx::tmem_ld_32x32b_x8(taddr + c0, v);
           ptx::tmem_wait_ld();
-          if (c0 + 32 >= T) {  // accumulator fully read: hand it back to the MMA warp
+          if (c0 + 8 >= T) {  // accumulator fully read: hand it back to the MMA warp
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acce[buf]));
           }
-          const int cnt = T - c0 < 32 ? T - c0 : 32;
+          const int cnt = T - c0 < 8 ? T - c0 : 8;
           const float* lgs = s_tlg + buf * 128 + c0;  // read as broadcasts
           float* y = p.ybuf + ((int64_t)sg.slot * p.M + t0 + c0) * p.N + n;
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj)
+          for (int jj = 0; jj < 8; ++jj)
             if (jj < cnt && n_ok) y[(int64_t)jj * p.N] = (__uint_as_float(v[jj]) + bias_n) * lgs[jj];
         }
       } else {  // 8 tokens per TMEM load: a quarter of the unrolled scatter code of 32 (C1 37.5 ->
