@@ -804,23 +804,24 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
           for (int jj = 0; jj < 8; ++jj)
             if (jj < cnt && n_ok) y[(int64_t)jj * p.N] = (__uint_as_float(v[jj]) + bias_n) * lgs[jj];
         }
-      } else {  // 8 tokens per TMEM load: a quarter of the unrolled scatter code of 32 (C1 37.5 ->
-                // 37.3 us, C2 80.6 -> 79.9, C5 1089.1 -> 1088.4)
+      } else {  // 16 tokens per TMEM load: half the unrolled scatter code of 32, half the TMEM
+                // round trips of 8 (32 -> 8 -> 16 tokens: C1 37.5 -> 37.3 -> 37.1 us,
+                // C2 80.6 -> 79.9 -> 79.8, C5 1089.1 -> 1088.4 -> 1086.7)
         float* o = p.out + n;
-        for (int c0 = 0; c0 < T; c0 += 8) {
-          uint32_t v[8];
-          ptx::tmem_ld_32x32b_x8(taddr + c0, v);
+        for (int c0 = 0; c0 < T; c0 += 16) {
+          uint32_t v[16];
+          ptx::tmem_ld_32x32b_x16(taddr + c0, v);
           ptx::tmem_wait_ld();
-          if (c0 + 8 >= T) {  // accumulator fully read: hand it back to the MMA warp
+          if (c0 + 16 >= T) {  // accumulator fully read: hand it back to the MMA warp
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acce[buf]));
           }
-          const int cnt = T - c0 < 8 ? T - c0 : 8;
+          const int cnt = T - c0 < 16 ? T - c0 : 16;
           const int32_t* rows = s_trow + buf * 128 + c0;  // read as broadcasts
           const float* lgs = s_tlg + buf * 128 + c0;
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
+          for (int jj = 0; jj < 16; ++jj) {
             if (jj < cnt) {
               const int row = rows[jj];
               if (n_ok && row >= 0) ptx::red_add_f32(o + (int64_t)row * p.N, (__uint_as_float(v[jj]) + bias_n) * lgs[jj]);
