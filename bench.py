@@ -730,16 +730,19 @@ def run_ours(args):
         "clocks": clocks,
         "wall_s_timed": t_wall,
     }
-    if not args.no_extras:
+    extras = set() if args.no_extras else set(args.extras.split(","))
+    if "configs" in extras:
         line["configs"] = _sub_workloads(args, flush, spec, d, prep)
+    if "route" in extras:
         line["route"] = _time_route(args, flush)
         if W.route_config(args.config).M == spec.M:
             line["layer"] = _time_layer(args, flush, prob, d, prep, ws, ms * 1e3, line["route"]["us_per_call"])
+    if "ffn" in extras:
         line["ffn"] = _time_ffn(args, flush)
-        if spec.x1_dtype != W.E2M1:
-            del prep
-            torch.cuda.empty_cache()
-            line["mxfp4"] = _time_mxfp4(args, flush)
+    if "mxfp4" in extras and spec.x1_dtype != W.E2M1:
+        del prep
+        torch.cuda.empty_cache()
+        line["mxfp4"] = _time_mxfp4(args, flush)
     if rank == 0 and not args.no_cpu_baseline:
         cgbs, cdt, sample, cores = _cpu_baseline(spec, inp)
         line["cpu_baseline"] = {"value": cgbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
@@ -767,6 +770,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the side measurements (the other workloads, routing step, SwiGLU FFN, MXFP4 operator)")
+    ap.add_argument("--extras", default="configs,route,ffn,mxfp4",
+                    help="which side measurements to run (comma list of configs, route, ffn, mxfp4; route adds the "
+                         "routing + operator layer when the workload has a routing shape)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

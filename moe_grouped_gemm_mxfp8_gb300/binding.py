@@ -20,7 +20,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = rang
 E4M3, E5M2 = 0, 1
 INDEX_I64, INDEX_I32 = 0, 1
 DETERMINISTIC = 1
-DEV_BAD_GROUP_LIST, DEV_BAD_ROW_INDEX, DEV_TIMEOUT = 1, 2, 4
+DEV_BAD_GROUP_LIST, DEV_BAD_ROW_INDEX, DEV_TIMEOUT, DEV_BAD_EXPERT_ID = 1, 2, 4, 8
 PROFILE_SLOTS = 5
 PROFILE_SLOT_NAMES = ("prep", "route", "gemm", "combine", "call")
 
@@ -34,7 +34,6 @@ ENTRY_POINTS = (
     "gmmfr_ffn_prepared_weights_size", "gmmfr_ffn_prepare_weights", "gmmfr_ffn_workspace_size",
     "gmmfr_llada2_moe_grouped_gemm",
 )
-DEV_BAD_EXPERT_ID = 8
 
 
 DT_U8, DT_E4M3, DT_E5M2, DT_E2M1X2, DT_E8M0, DT_I64, DT_I32, DT_F32, DT_BF16 = range(9)

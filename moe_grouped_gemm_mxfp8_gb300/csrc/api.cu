@@ -91,9 +91,10 @@ int device_sms() {
   return sms;
 }
 
-// Testing aids for the deterministic mode's schedule: GMMFR_GRID = the grouped GEMM's CTA count
-// (1 .. 1023; default one per SM), GMMFR_REVERSE_UNITS = 1 makes each CTA walk its units last to
-// first.  Neither changes the K split, so neither may change a bit of the result.
+// Testing aids for the grouped GEMM's schedule: GMMFR_GRID = its CTA count (1 .. 1023; default
+// one per SM), GMMFR_REVERSE_UNITS = 1 makes each CTA walk its units last to first (deterministic
+// mode).  Neither changes the K split, so in deterministic mode neither may change a bit of the
+// result; in atomic mode the grid moves the stream-K cuts.
 int grid_override() {
   if (const char* s = std::getenv("GMMFR_GRID")) {
     const int v = std::atoi(s);

@@ -415,27 +415,28 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
       if (!epi_all(ok)) break;  // the 4 warps leave together: they share a named barrier
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * tmax;
-      for (int c0 = 0; c0 < T; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(taddr + c0, v);
+      // 16 tokens per TMEM load: half the unrolled code of 32 (model shape 258.8 -> 256.4 us)
+      for (int c0 = 0; c0 < T; c0 += 16) {
+        uint32_t v[16];
+        ptx::tmem_ld_32x32b_x16(taddr + c0, v);
         ptx::tmem_wait_ld();
-        if (c0 + 32 >= T) {
+        if (c0 + 16 >= T) {
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acce[buf]));
         }
-        const int cnt = T - c0 < 32 ? T - c0 : 32;
+        const int cnt = T - c0 < 16 ? T - c0 : 16;
         if constexpr (kGateUp) {
           // lanes of quadrants 2, 3 hold the up columns matching quadrants 0, 1
           if (q >= 2) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) xchg[((q - 2) * 32 + jj) * 32 + lane] = __uint_as_float(v[jj]);
+            for (int jj = 0; jj < 16; ++jj) xchg[((q - 2) * 32 + jj) * 32 + lane] = __uint_as_float(v[jj]);
           }
           epi_bar();
           if (q < 2) {
             const int64_t col = (int64_t)j * 64 + q * 32 + lane;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
+            for (int jj = 0; jj < 16; ++jj) {
               if (jj < cnt && col < p.out_cols) {
                 const float gt = __uint_as_float(v[jj]);
                 const float up = xchg[(q * 32 + jj) * 32 + lane];
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(ffn::kThreads, 1)
         } else {
           const int64_t col = (int64_t)j * kTileN + q * 32 + lane;
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj)
+          for (int jj = 0; jj < 16; ++jj)
             if (jj < cnt && col < p.out_cols)
               p.out[((int64_t)t0 + c0 + jj) * p.out_cols + col] = __float2bfloat16_rn(__uint_as_float(v[jj]));
         }

@@ -785,8 +785,9 @@ __global__ void __launch_bounds__(gemm_threads(fp4), 1)
       const float bias_n = (p.bias != nullptr && sg.kb0 == 0 && n_ok) ? bf16f(p.bias[(int64_t)e * p.N + n]) : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * tmax;
       // one loop per mode, so the atomic mode's hot code holds no store path of the
-      // deterministic one (the instruction cache is the scarce resource here); 8 tokens per TMEM
-      // load in both, a quarter of the unrolled code of 32 (deterministic C5 1150 -> 1147 us)
+      // deterministic one (the instruction cache is the scarce resource here); the store path
+      // takes 8 tokens per TMEM load, a quarter of the unrolled code of 32 (deterministic C5
+      // 1150 -> 1147 us; 16 tokens measured no better)
       if constexpr (det) {  // stored into the per-token buffer
         for (int c0 = 0; c0 < T; c0 += 8) {
           uint32_t v[8];

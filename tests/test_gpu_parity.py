@@ -164,6 +164,17 @@ SMALL = {
     "mxfp4_straddle": dict(E=9, M=1344, batch=200, N=256, K=128, rows="random", x1_dtype=W.E2M1,
                            x2_dtype=W.E2M1, counts="explicit",
                            explicit_counts=(63, 64, 65, 127, 128, 129, 255, 256, 257)),
+    # many short segments per CTA (2 K blocks per column tile, 27 items per CTA), 256 and 257
+    # experts (the decode's chunked scan), empty experts under both group_list encodings next to
+    # experts of exactly 32 tokens (one 32-row box)
+    "short_segments": dict(E=64, M=512, batch=512, N=4096, K=256, rows="random"),
+    "e256_multinomial": dict(E=256, M=2048, batch=512, N=256, K=384, counts="multinomial", rows="random",
+                             transpose_x2=True),
+    "e257": dict(E=257, M=2056, batch=512, N=256, K=384, rows="random"),
+    "empty_prefix": dict(E=7, M=90, batch=40, N=512, K=512, group_list_type=0, rows="random",
+                         counts="explicit", explicit_counts=(0, 32, 5, 0, 17, 1, 32), out_init="randn"),
+    "empty_counts": dict(E=7, M=90, batch=40, N=512, K=512, rows="random", shared_rows=8, shared_offset=3,
+                         counts="explicit", explicit_counts=(32, 0, 0, 25, 1, 32, 0)),
 }
 
 
@@ -189,6 +200,16 @@ def test_small_deterministic(name):
 @pytest.mark.parametrize("case", ["straddle", "mxfp4_straddle"])
 def test_token_group_widths(tmax, case, monkeypatch):
     monkeypatch.setenv("GMMFR_TMAX", tmax)
+    spec = _spec(**SMALL[case])
+    check_full(spec, W.make_inputs(spec))
+
+
+@pytest.mark.parametrize("grid", ["1", "37", "300"])
+@pytest.mark.parametrize("case", ["short_segments", "empty_prefix"])
+def test_atomic_grids(grid, case, monkeypatch):
+    """Atomic mode for any CTA count: one CTA holding every item (the ring wrapping many
+    times), CTAs holding ragged item counts, and more CTAs than SMs (two waves)."""
+    monkeypatch.setenv("GMMFR_GRID", grid)
     spec = _spec(**SMALL[case])
     check_full(spec, W.make_inputs(spec))
 
