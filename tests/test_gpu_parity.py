@@ -456,7 +456,10 @@ def _schedules():
            [dict(GMMFR_GRID=str(g), GMMFR_REVERSE_UNITS="1") for g in (37, sms)]
 
 
-@pytest.mark.parametrize("case", ["config4", "straddle", "bias_split_k", "mxfp4_t", "ragged_counts"])
+# config4, straddle, k200 and mxfp4_straddle hold token groups of 64 or 128, the others groups of
+# at most 32
+@pytest.mark.parametrize("case", ["config4", "straddle", "k200", "mxfp4_straddle", "bias_split_k", "mxfp4_t",
+                                  "ragged_counts"])
 def test_deterministic_bits_do_not_depend_on_the_schedule(case, monkeypatch):
     """Deterministic mode (aclnn V3, 确定性计算) gives the same bits whatever the number of
     CTAs (1, 37, one per SM) and whichever order each CTA takes its units in."""
