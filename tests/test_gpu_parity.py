@@ -175,6 +175,15 @@ SMALL = {
                          counts="explicit", explicit_counts=(0, 32, 5, 0, 17, 1, 32), out_init="randn"),
     "empty_counts": dict(E=7, M=90, batch=40, N=512, K=512, rows="random", shared_rows=8, shared_offset=3,
                          counts="explicit", explicit_counts=(32, 0, 0, 25, 1, 32, 0)),
+    # the expert limit (1024: the decode's scans carry over five chunks of its threads), with
+    # empty experts, under both group_list encodings, and with Zipf-sized groups (token groups of
+    # 128 and the cost-weighted split over 1024 experts)
+    "e1024": dict(E=1024, M=3000, batch=1000, N=256, K=256, counts="multinomial", rows="random"),
+    "e1024_zipf_prefix": dict(E=1024, M=4000, batch=1000, N=192, K=384, counts="zipf", group_list_type=0,
+                              rows="random", out_init="randn"),
+    # many routed tokens (40000: 300-odd token groups of up to 128 in a few large experts)
+    "many_tokens": dict(E=16, M=40000, batch=8192, N=256, K=256, counts="zipf", zipf_s=0.8, rows="random",
+                        shared_rows=64, shared_offset=100),
 }
 
 
@@ -187,7 +196,8 @@ def test_small_atomic(name):
 # scalar path
 @pytest.mark.parametrize("name", ["basic", "transposed", "ragged_counts", "random_rows_shared", "straddle", "k96",
                                   "bias_split_k", "mxfp4_t", "mxfp4_k352_bias", "k16_n1", "mxfp4_k96",
-                                  "e4m3_tokens_mxfp4_weights", "k72_t", "k1032_split", "mxfp4_k40"])
+                                  "e4m3_tokens_mxfp4_weights", "k72_t", "k1032_split", "mxfp4_k40", "e1024",
+                                  "e1024_zipf_prefix", "many_tokens"])
 def test_small_deterministic(name):
     spec = _spec(**SMALL[name])
     inp = W.make_inputs(spec)
