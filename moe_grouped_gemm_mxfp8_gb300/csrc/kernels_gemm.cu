@@ -162,14 +162,22 @@ struct Groups {
 };
 
 // The sequence of (group, tile, K range) segments of one CTA; every role walks it.
-// Tiles are ordered column-tile-major (tile = j * n_groups + g), so the token
-// groups of one expert that holds more than tmax tokens are adjacent and their
-// shared weight tiles are re-read while still in L2.
+// With the even split (token groups of at most 32) the atomic mode orders the items
+// group-major (tile = g * NT + j): a CTA's range then reads an expert's prepared tiles in
+// address order, the order bulk copies stream fastest in, and keeps each group's token rows
+// for all its column tiles (C5 1086 -> 1076 us against column-tile-major order).  With the
+// cost-weighted split, and in deterministic mode, tiles stay column-tile-major
+// (tile = j * n_groups + g), so the groups of one expert that holds more than tmax tokens
+// are adjacent and re-read their shared weight tiles while still in L2 (group-major cost
+// C4 11 us).  The walk steps (major, minor) = (g, j) or (j, g) with selects, not branches.
 struct Sched {
   int64_t i, i_end, step;
   int NT, KB, split, ng;
   bool det;
-  int cur_g, cur_j, cur_kb;  // group, column tile and K block of item i (deterministic: K split)
+  bool gmajor;               // atomic mode, even split: tile = g * NT + j
+  // item i's K block (deterministic: K split) and tile: deterministic mode cur_g = group and
+  // cur_j = column tile; atomic mode cur_g = the major and cur_j = the minor tile index
+  int cur_g, cur_j, cur_kb;
   __device__ void init(int n_groups, int NT_, int KB_, bool det_, int split_, bool reverse, const Groups& gr) {
     ng = n_groups;
     NT = NT_;
@@ -194,7 +202,8 @@ struct Sched {
       return;
     }
     step = 0;
-    if (gr.wbase[gr.E] > 0) {
+    gmajor = gr.wbase[gr.E] <= 0;
+    if (!gmajor) {
       // equal cost per CTA: items of large token groups move more bytes than those of small ones
       const int64_t total = (int64_t)NT * KB * gr.wbase[gr.E];
       i = gr.item_at(total * blockIdx.x / gridDim.x, KB, NT, n_groups);
@@ -209,28 +218,30 @@ struct Sched {
         i_end = total * (blockIdx.x + 1) / gridDim.x;
       }
     }
-    // position of the first item; next() then walks tiles without dividing
+    // position of the first item (tile = major * minors + minor); next() then walks tiles
+    // without dividing.  cur_g holds the major index, cur_j the minor one.
     const int64_t tile = i / KB;
     cur_kb = (int)(i - tile * KB);
-    cur_g = (int)(tile % (ng > 0 ? ng : 1));
-    cur_j = (int)(tile / (ng > 0 ? ng : 1));
+    const int64_t minors = gmajor ? NT : (ng > 0 ? ng : 1);
+    cur_g = (int)(tile / minors);
+    cur_j = (int)(tile - cur_g * minors);
   }
   // kDet: the kernel's mode (compile time, so each instantiation holds one walk)
   template <bool kDet>
   __device__ __forceinline__ bool next(Seg& s) {
     if (i >= i_end) return false;
-    if constexpr (!kDet) {  // tiles in order j * n_groups + g; a segment runs to its tile's end or the range's
-      s.g = cur_g;
-      s.j = cur_j;
+    if constexpr (!kDet) {  // tiles in (major, minor) order; a segment runs to its tile's end or the range's
+      s.g = gmajor ? cur_g : cur_j;
+      s.j = gmajor ? cur_j : cur_g;
       s.kb0 = cur_kb;
       const int64_t left = i_end - i;
       s.kb1 = (KB - cur_kb) < left ? KB : cur_kb + (int)left;
       s.slot = 0;
       i += s.kb1 - s.kb0;
       cur_kb = 0;
-      if (++cur_g == ng) {
-        cur_g = 0;
-        ++cur_j;
+      if (++cur_j == (gmajor ? NT : ng)) {
+        cur_j = 0;
+        ++cur_g;
       }
       return true;
     } else {  // deterministic: the next (group, tile, K split) unit of this CTA's range
