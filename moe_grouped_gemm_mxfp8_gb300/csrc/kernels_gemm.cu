@@ -165,18 +165,20 @@ struct Groups {
 // With the even split (token groups of at most 32) the atomic mode orders the items
 // group-major (tile = g * NT + j): a CTA's range then reads an expert's prepared tiles in
 // address order, the order bulk copies stream fastest in, and keeps each group's token rows
-// for all its column tiles (C5 1086 -> 1076 us against column-tile-major order).  With the
-// cost-weighted split, and in deterministic mode, tiles stay column-tile-major
-// (tile = j * n_groups + g), so the groups of one expert that holds more than tmax tokens
-// are adjacent and re-read their shared weight tiles while still in L2 (group-major cost
-// C4 11 us).  The walk steps (major, minor) = (g, j) or (j, g) with selects, not branches.
+// for all its column tiles (C5 1086 -> 1076 us against column-tile-major order); deterministic
+// mode's units (tile, then K split) follow the same order when every expert is one group.
+// With the cost-weighted split, or token groups wider than 32 in deterministic mode, tiles
+// stay column-tile-major (tile = j * n_groups + g), so the groups of one expert that holds more
+// than tmax tokens are adjacent and re-read their shared weight tiles while still in L2
+// (group-major cost C4 11 us).  The walk steps (major, minor) = (g, j) or (j, g) with selects,
+// not branches.
 struct Sched {
   int64_t i, i_end, step;
   int NT, KB, split, ng;
   bool det;
   bool gmajor;               // atomic mode, even split: tile = g * NT + j
-  // item i's K block (deterministic: K split) and tile: deterministic mode cur_g = group and
-  // cur_j = column tile; atomic mode cur_g = the major and cur_j = the minor tile index
+  // item i's K block (deterministic mode: K split) and tile: cur_g = the major and cur_j = the
+  // minor tile index (group and column tile, or column tile and group)
   int cur_g, cur_j, cur_kb;
   __device__ void init(int n_groups, int NT_, int KB_, bool det_, int split_, bool reverse, const Groups& gr) {
     ng = n_groups;
@@ -197,8 +199,10 @@ struct Sched {
       const int64_t first = reverse && i_end > i ? i_end - 1 : i;
       const int64_t tile = first / split;
       cur_kb = (int)(first - tile * split);
-      cur_g = (int)(tile % (ng > 0 ? ng : 1));
-      cur_j = (int)(tile / (ng > 0 ? ng : 1));
+      gmajor = gr.tmax <= 32;  // one token group per expert: group-major, as in atomic mode
+      const int64_t minors = gmajor ? NT : (ng > 0 ? ng : 1);
+      cur_g = (int)(tile / minors);
+      cur_j = (int)(tile - cur_g * minors);
       return;
     }
     step = 0;
@@ -246,25 +250,26 @@ struct Sched {
       return true;
     } else {  // deterministic: the next (group, tile, K split) unit of this CTA's range
       const int sp = cur_kb;
-      s.g = cur_g;
-      s.j = cur_j;
+      s.g = gmajor ? cur_g : cur_j;
+      s.j = gmajor ? cur_j : cur_g;
       s.kb0 = (int)((int64_t)sp * KB / split);
       s.kb1 = (int)((int64_t)(sp + 1) * KB / split);
       s.slot = sp;
       ++i;
+      const int minors = gmajor ? NT : ng;
       if (step > 0) {
         if (++cur_kb == split) {
           cur_kb = 0;
-          if (++cur_g == ng) {
-            cur_g = 0;
-            ++cur_j;
+          if (++cur_j == minors) {
+            cur_j = 0;
+            ++cur_g;
           }
         }
       } else if (--cur_kb < 0) {
         cur_kb = split - 1;
-        if (--cur_g < 0) {
-          cur_g = ng - 1;
-          --cur_j;
+        if (--cur_j < 0) {
+          cur_j = minors - 1;
+          --cur_g;
         }
       }
       return true;
