@@ -214,6 +214,20 @@ def test_token_group_widths(tmax, case, monkeypatch):
     check_full(spec, W.make_inputs(spec))
 
 
+@pytest.mark.parametrize("tmax", ["32", "128"])
+@pytest.mark.parametrize("case", ["straddle", "mxfp4_straddle"])
+def test_token_group_widths_deterministic(tmax, case, monkeypatch):
+    """Deterministic mode with the group width forced: 32 puts experts of up to 257 tokens into
+    many 32-token groups (walked group-major, sibling groups far apart), 128 into few; both match
+    the oracle and repeat their bits."""
+    monkeypatch.setenv("GMMFR_TMAX", tmax)
+    spec = _spec(**SMALL[case])
+    inp = W.make_inputs(spec)
+    got, _ = check_full(spec, inp, deterministic=True)
+    again, _ = gpu_run(spec, inp, deterministic=True)
+    assert np.array_equal(got, again)
+
+
 @pytest.mark.parametrize("grid", ["1", "37", "300"])
 @pytest.mark.parametrize("case", ["short_segments", "empty_prefix"])
 def test_atomic_grids(grid, case, monkeypatch):
